@@ -1,0 +1,317 @@
+// CPU oracle of the HiSparse-style decode KV swap-in.
+//
+// TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+// benchmark's CPU-baseline leg may load this file's library.  The CUDA
+// library never includes, links or calls it, and the two share no code.
+//
+// What it computes, step by step, with the passage each step follows:
+//
+//  * The call resolves every (request, step, k) entry of the indexer's top-k
+//    against a per-request device hot buffer, treating all speculative steps
+//    of one call as one working set ("[HiSparse] Support hisparse multi-step
+//    swap io kernel", section 功能与动机; section 实现拆解 item 1: gather
+//    flattens [batch, steps, top_k], looks tokens up in a token-to-slot hash,
+//    de-duplicates misses across steps and copies each unique miss to a
+//    scratch device location).
+//  * Commit, per request: CLOCK update of the hot cache, rotation of scratch
+//    and hot locations, token-to-slot map update, resolution of overflowing
+//    misses (same section, item 1).  Reference epochs are kept per slot
+//    (same page, 关键源码片段: per-request reference-epoch rows).
+//  * When the unique-miss union exceeds what the cache can take, admission
+//    becomes approximate and prefers the most recent speculative step; the
+//    current call stays data-exact (same page, 风险与影响).
+//  * The original single-step kernel loads missing rows from the CPU copy of
+//    the KV cache and updates an LRU (PR #20343 summary, 实现拆解 and 功能与动机).
+//
+// Readings where the pages leave a step open (each one is a choice of this
+// build, stated here so that a reader can check the code against it):
+//  1. The reference mark of a slot is the epoch of the last call that
+//     referenced it; one epoch per call.  Victims are the non-hit slots with
+//     the smallest (epoch, slot) pairs: never-used slots (epoch -1) first,
+//     then least recently used, ties to the lowest slot.  With one token per
+//     call this is exactly LRU.
+//  2. An entry is valid iff 0 <= t < min(seq_len, L_max); invalid entries get
+//     location -1, change nothing and count only as "invalid".
+//  3. Misses are numbered j = 0, 1, ... in order of first occurrence in
+//     (step, k) order; miss j is written to physical row phys[H + j] of the
+//     request's buffer region (the scratch ring, C = max_steps * top_k rows).
+//  4. cap = H - (distinct hit slots); m = min(U, cap).  If U <= cap every
+//     miss is admitted; otherwise the m misses ranked highest by (last step
+//     in which the token occurs descending, j ascending) are admitted.
+//  5. The admitted misses in ascending j are paired with the victims in
+//     ascending slot order; a pair (j, v) swaps phys[v] and phys[H + j], so
+//     the copied row becomes the hot row without a second copy.
+//  6. Locations are int32 rows of the layer's device buffer:
+//     q * (H + C) + phys[position].
+#include "hs_oracle.h"
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <numeric>
+#include <set>
+#include <thread>
+#include <unordered_map>
+#include <vector>
+
+namespace {
+
+struct RequestCache {
+    std::unordered_map<int32_t, int32_t> res;  // resident token -> hot slot
+    std::vector<int32_t> tok;                  // [H] token held by slot, -1 empty
+    std::vector<int32_t> ep;                   // [H] epoch of last reference, -1 never
+    std::vector<int32_t> phys;                 // [H + C] physical row of each position
+    int32_t epoch = 0;                         // epoch of the next call
+};
+
+}  // namespace
+
+struct hso_oracle {
+    int32_t R, L, W, H, K, S_max, layers, C;
+    std::vector<RequestCache> cache;  // [layers * R]
+
+    RequestCache& at(int32_t layer, int32_t q) { return cache[(size_t)layer * R + q]; }
+    const RequestCache& at(int32_t layer, int32_t q) const { return cache[(size_t)layer * R + q]; }
+};
+
+namespace {
+
+void make_empty(const hso_oracle& o, RequestCache& rc) {
+    rc.res.clear();
+    rc.tok.assign(o.H, -1);
+    rc.ep.assign(o.H, -1);
+    rc.phys.resize(o.H + o.C);
+    std::iota(rc.phys.begin(), rc.phys.end(), 0);
+    rc.epoch = 0;
+}
+
+// One request of one call.  Follows readings 1-6 in the file header.
+void swap_in_request(const hso_oracle& o, RequestCache& rc, int32_t q, const int32_t* topk_b,
+                     int32_t S, int32_t seq_len, const uint8_t* host_pool, uint8_t* device_kv,
+                     int32_t* locs_b, int32_t* st, int64_t* src_b, int64_t* dst_b,
+                     int32_t* count_b) {
+    const int32_t H = o.H, C = o.C, K = o.K, W = o.W;
+    const int64_t base = (int64_t)q * (H + C);
+    const int32_t limit = std::min(seq_len, o.L);
+    const int32_t E = rc.epoch;
+
+    int32_t stat[HSO_NUM_STATS] = {0};
+    std::vector<int32_t> U;                      // unique misses, first-occurrence order
+    std::vector<int32_t> last_step;              // last step in which miss j occurs
+    std::unordered_map<int32_t, int32_t> first;  // missing token -> ordinal j
+    std::set<int32_t> hit_slots;
+
+    // Gather: classify each entry in (step, k) order and return its location.
+    for (int32_t s = 0; s < S; ++s) {
+        for (int32_t k = 0; k < K; ++k) {
+            const int32_t i = s * K + k;
+            const int32_t t = topk_b[i];
+            if (t < 0 || t >= limit) {
+                locs_b[i] = -1;
+                stat[HSO_STAT_INVALID]++;
+                continue;
+            }
+            auto r = rc.res.find(t);
+            if (r != rc.res.end()) {
+                const int32_t v = r->second;
+                hit_slots.insert(v);
+                locs_b[i] = (int32_t)(base + rc.phys[v]);
+                stat[HSO_STAT_HITS]++;
+                continue;
+            }
+            auto f = first.find(t);
+            if (f != first.end()) {
+                const int32_t j = f->second;
+                last_step[j] = s;
+                locs_b[i] = (int32_t)(base + rc.phys[H + j]);
+                stat[HSO_STAT_DUP_MISSES]++;
+                continue;
+            }
+            const int32_t j = (int32_t)U.size();
+            first[t] = j;
+            U.push_back(t);
+            last_step.push_back(s);
+            const int64_t dst_row = base + rc.phys[H + j];
+            const int64_t src_row = (int64_t)q * o.L + t;
+            std::memcpy(device_kv + dst_row * W, host_pool + src_row * W, (size_t)W);
+            locs_b[i] = (int32_t)dst_row;
+            if (src_b) src_b[j] = src_row;
+            if (dst_b) dst_b[j] = dst_row;
+        }
+    }
+    if (count_b) *count_b = (int32_t)U.size();
+
+    // Commit 1: every hot slot referenced by this call takes the call's epoch.
+    for (int32_t v : hit_slots) rc.ep[v] = E;
+
+    // Commit 2: how many misses the cache can take without evicting a hit.
+    const int32_t nU = (int32_t)U.size();
+    const int32_t cap = H - (int32_t)hit_slots.size();
+    const int32_t m = std::min(nU, cap);
+
+    // Commit 3: which misses are admitted (reading 4).
+    std::vector<int32_t> adm(nU);
+    std::iota(adm.begin(), adm.end(), 0);
+    if (nU > cap) {
+        std::stable_sort(adm.begin(), adm.end(), [&](int32_t a, int32_t b) {
+            if (last_step[a] != last_step[b]) return last_step[a] > last_step[b];
+            return a < b;
+        });
+        adm.resize(m);
+        std::sort(adm.begin(), adm.end());
+    }
+
+    // Commit 4: victims are the m non-hit slots with the smallest (epoch, slot).
+    std::vector<int32_t> cand;
+    for (int32_t v = 0; v < H; ++v)
+        if (!hit_slots.count(v)) cand.push_back(v);
+    std::sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
+        if (rc.ep[a] != rc.ep[b]) return rc.ep[a] < rc.ep[b];
+        return a < b;
+    });
+    cand.resize(m);
+    std::sort(cand.begin(), cand.end());
+
+    // Commit 5: rotate each admitted scratch row into its victim's hot slot.
+    for (int32_t i = 0; i < m; ++i) {
+        const int32_t j = adm[i];
+        const int32_t v = cand[i];
+        if (rc.tok[v] != -1) {
+            rc.res.erase(rc.tok[v]);
+            stat[HSO_STAT_EVICTED]++;
+        }
+        std::swap(rc.phys[v], rc.phys[H + j]);
+        rc.tok[v] = U[j];
+        rc.res[U[j]] = v;
+        rc.ep[v] = E;
+    }
+    rc.epoch = E + 1;
+
+    stat[HSO_STAT_HIT_SLOTS] = (int32_t)hit_slots.size();
+    stat[HSO_STAT_UNIQUE_MISSES] = nU;
+    stat[HSO_STAT_ADMITTED] = m;
+    stat[HSO_STAT_OVERFLOW] = nU - m;
+    if (st) std::memcpy(st, stat, sizeof(stat));
+}
+
+}  // namespace
+
+extern "C" {
+
+hso_oracle* hso_create(int32_t num_requests, int32_t max_seq_len, int32_t item_size_bytes,
+                       int32_t hot_buffer_size, int32_t top_k, int32_t max_steps,
+                       int32_t num_layers) {
+    if (num_requests <= 0 || max_seq_len <= 0 || item_size_bytes <= 0 || hot_buffer_size <= 0 ||
+        top_k <= 0 || max_steps <= 0 || num_layers <= 0)
+        return nullptr;
+    hso_oracle* o = new hso_oracle;
+    o->R = num_requests;
+    o->L = max_seq_len;
+    o->W = item_size_bytes;
+    o->H = hot_buffer_size;
+    o->K = top_k;
+    o->S_max = max_steps;
+    o->layers = num_layers;
+    o->C = max_steps * top_k;
+    o->cache.resize((size_t)num_layers * num_requests);
+    for (auto& rc : o->cache) make_empty(*o, rc);
+    return o;
+}
+
+void hso_destroy(hso_oracle* o) { delete o; }
+
+int hso_swap_in(hso_oracle* o, int32_t layer, const uint8_t* host_pool, uint8_t* device_kv,
+                const int32_t* req_pool_indices, const int32_t* seq_lens, const int32_t* topk,
+                int32_t batch, int32_t num_steps, int32_t* device_locs, int32_t* stats,
+                int64_t* miss_src, int64_t* miss_dst, int32_t* miss_count,
+                int32_t num_threads) {
+    if (!o || layer < 0 || layer >= o->layers || batch < 0 || num_steps < 1 ||
+        num_steps > o->S_max)
+        return HSO_ERR_ARG;
+    if (batch == 0) return HSO_OK;
+    if (!host_pool || !device_kv || !req_pool_indices || !seq_lens || !topk || !device_locs)
+        return HSO_ERR_ARG;
+    std::set<int32_t> seen;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t q = req_pool_indices[b];
+        if (q < 0 || q >= o->R) return HSO_ERR_ARG;
+        if (!seen.insert(q).second) return HSO_ERR_DUPLICATE_REQUEST;
+    }
+    const int64_t per_b = (int64_t)num_steps * o->K;
+    auto run = [&](int32_t b) {
+        const int32_t q = req_pool_indices[b];
+        swap_in_request(*o, o->at(layer, q), q, topk + b * per_b, num_steps, seq_lens[b],
+                        host_pool, device_kv, device_locs + b * per_b,
+                        stats ? stats + (int64_t)b * HSO_NUM_STATS : nullptr,
+                        miss_src ? miss_src + (int64_t)b * o->C : nullptr,
+                        miss_dst ? miss_dst + (int64_t)b * o->C : nullptr,
+                        miss_count ? miss_count + b : nullptr);
+    };
+    if (num_threads <= 1 || batch == 1) {
+        for (int32_t b = 0; b < batch; ++b) run(b);
+    } else {
+        // Requests are independent: each owns its cache state and its rows.
+        const int32_t n = std::min(num_threads, batch);
+        std::vector<std::thread> pool;
+        for (int32_t w = 0; w < n; ++w)
+            pool.emplace_back([&, w] {
+                for (int32_t b = w; b < batch; b += n) run(b);
+            });
+        for (auto& th : pool) th.join();
+    }
+    return HSO_OK;
+}
+
+int hso_get_request_state(const hso_oracle* o, int32_t layer, int32_t q, int32_t* tok,
+                          int32_t* ep, int32_t* phys, int32_t* epoch) {
+    if (!o || layer < 0 || layer >= o->layers || q < 0 || q >= o->R) return HSO_ERR_ARG;
+    const RequestCache& rc = o->at(layer, q);
+    if (tok) std::memcpy(tok, rc.tok.data(), sizeof(int32_t) * o->H);
+    if (ep) std::memcpy(ep, rc.ep.data(), sizeof(int32_t) * o->H);
+    if (phys) std::memcpy(phys, rc.phys.data(), sizeof(int32_t) * (o->H + o->C));
+    if (epoch) *epoch = rc.epoch;
+    return HSO_OK;
+}
+
+int hso_reset_requests(hso_oracle* o, const int32_t* req_pool_indices, int32_t n) {
+    if (!o || n < 0 || (n > 0 && !req_pool_indices)) return HSO_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (req_pool_indices[i] < 0 || req_pool_indices[i] >= o->R) return HSO_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        for (int32_t l = 0; l < o->layers; ++l) make_empty(*o, o->at(l, req_pool_indices[i]));
+    return HSO_OK;
+}
+
+// Sparse page table: the pages holding a request's selected tokens, sorted
+// ascending, and for each entry its position in the gathered pages
+// (page index in that list * page_size + offset in page).  Follows
+// "SGLang HiSparse" sections 1.2 and 2.3 (PAGED mode: token -> page plus
+// in-page offset; only pages holding selected tokens reach attention).
+int hso_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t batch,
+                   int32_t num_steps, int32_t top_k, int32_t page_size, int32_t* pages,
+                   int32_t* num_pages, int32_t* token_page) {
+    if (batch < 0 || num_steps < 1 || top_k < 1 || page_size < 1) return HSO_ERR_ARG;
+    const int64_t n = (int64_t)num_steps * top_k;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int32_t* t_b = topk + b * n;
+        std::map<int32_t, int32_t> index;  // page -> position in the sorted list
+        for (int64_t i = 0; i < n; ++i)
+            if (t_b[i] >= 0 && t_b[i] < seq_lens[b]) index[t_b[i] / page_size] = 0;
+        int32_t p = 0;
+        for (auto& kv : index) {
+            pages[b * n + p] = kv.first;
+            kv.second = p++;
+        }
+        for (int64_t i = p; i < n; ++i) pages[b * n + i] = -1;
+        num_pages[b] = p;
+        for (int64_t i = 0; i < n; ++i) {
+            const int32_t t = t_b[i];
+            token_page[b * n + i] = (t >= 0 && t < seq_lens[b])
+                                        ? index[t / page_size] * page_size + t % page_size
+                                        : -1;
+        }
+    }
+    return HSO_OK;
+}
+
+}  // extern "C"

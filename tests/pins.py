@@ -1,0 +1,223 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each routine takes a loaded oracle library (so that the mutation test can
+run the same pins against deliberately broken builds) and raises
+AssertionError on a mismatch.
+
+  pin_lru:            with one token per call, epoch-CLOCK with a lowest-slot
+                      tie-break must equal textbook LRU (an OrderedDict);
+  pin_first_call:     closed forms of the first call on an empty cache;
+  pin_repeat_call:    repeating a call that fits is all hits, same locations;
+  pin_invariants:     random tiny sweeps checked with the property checker;
+  pin_simulator:      random tiny sweeps equal the brute-force list model;
+  pin_overflow:       overflow cases checked with the property checker;
+  pin_782:            the multi-step report's test shape: 782 cross-step
+                      unique misses at batch 1 (section 实现拆解 item 4);
+  pin_page_table:     sparse page table equals np.unique of the pages.
+"""
+from __future__ import annotations
+
+from collections import OrderedDict
+
+import numpy as np
+
+from common import OracleHarness
+from simulator import ListCache
+
+WIDTH = 32  # tiny rows for the CPU pins (the real rows are 656 bytes)
+
+
+def pin_lru(lib, trials: int = 12, calls: int = 120) -> None:
+    rng = np.random.default_rng(7)
+    for trial in range(trials):
+        H = int(rng.integers(1, 9))
+        universe = int(rng.integers(H + 1, 3 * H + 4))
+        h = OracleHarness(1, 64, WIDTH, H, 1, 1, lib=lib)
+        lru = OrderedDict()
+        for c in range(calls):
+            t = int(rng.integers(0, universe))
+            out = h.call(np.array([[[t]]], np.int32), np.array([0], np.int32),
+                         np.array([64], np.int32))
+            hit = t in lru
+            st = out["stats"][0]
+            assert st[0] == int(hit), "LRU hit/miss differs at call %d" % c
+            if hit:
+                lru.move_to_end(t)
+            else:
+                if len(lru) == H:
+                    lru.popitem(last=False)
+                lru[t] = None
+            res = set(int(x) for x in out["after"][0]["tok"] if x != -1)
+            assert res == set(lru), "resident set differs from LRU at call %d" % c
+
+
+def pin_first_call(lib) -> None:
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        R, H, K, S = 3, int(rng.integers(4, 40)), int(rng.integers(1, 9)), int(rng.integers(1, 5))
+        C = S * K
+        L = 50
+        h = OracleHarness(R, L, WIDTH, H, K, S, lib=lib)
+        topk = rng.integers(-3, L + 3, size=(2, S, K)).astype(np.int32)
+        rpi = np.array([2, 0], np.int32)
+        sl = np.array([L, 30], np.int32)
+        out = h.call(topk, rpi, sl)
+        for b in range(2):
+            q = int(rpi[b])
+            flat = topk[b].reshape(-1)
+            valid = [t for t in flat.tolist() if 0 <= t < sl[b]]
+            distinct = list(dict.fromkeys(valid))
+            assert out["stats"][b][3] == len(distinct)
+            first = {t: j for j, t in enumerate(distinct)}
+            for i, t in enumerate(flat.tolist()):
+                want = q * (H + C) + H + first[t] if t in first else -1
+                assert out["locs"][b].reshape(-1)[i] == want
+            st = out["after"][q]
+            m = min(len(distinct), H)
+            # empty slots have the oldest mark, so the first m slots take misses 0..m-1
+            assert st["tok"][:m].tolist() == distinct[:m] or len(distinct) > H
+            if len(distinct) <= H:
+                assert (st["tok"][m:] == -1).all()
+
+
+def pin_repeat_call(lib) -> None:
+    rng = np.random.default_rng(13)
+    for trial in range(20):
+        H, K, S = int(rng.integers(8, 40)), int(rng.integers(1, 9)), int(rng.integers(1, 5))
+        h = OracleHarness(2, 64, WIDTH, H, K, S, lib=lib)
+        topk = rng.integers(0, 64, size=(2, S, K)).astype(np.int32)
+        rpi = np.array([1, 0], np.int32)
+        sl = np.array([64, 64], np.int32)
+        first = h.call(topk, rpi, sl)
+        again = h.call(topk, rpi, sl)
+        for b in range(2):
+            if first["stats"][b][3] <= H:
+                assert again["stats"][b][3] == 0
+                assert (again["locs"][b] == first["locs"][b]).all()
+
+
+def _random_call(rng, B, R, S, K, L):
+    topk = rng.integers(-2, L + 2, size=(B, S, K)).astype(np.int32)
+    # bias towards reuse so that hits, duplicates and evictions all occur
+    small = rng.integers(0, max(2, L // 3), size=(B, S, K)).astype(np.int32)
+    pick = rng.random((B, S, K)) < 0.5
+    topk[pick] = small[pick]
+    rpi = rng.permutation(R)[:B].astype(np.int32)
+    sl = rng.integers(max(1, L // 2), L + 3, size=B).astype(np.int32)
+    return topk, rpi, sl
+
+
+def pin_invariants(lib, trials: int = 25, calls: int = 6) -> None:
+    rng = np.random.default_rng(17)
+    for trial in range(trials):
+        H = int(rng.integers(1, 9))
+        K = int(rng.integers(1, 9))
+        S_max = int(rng.integers(1, 5))
+        R = int(rng.integers(1, 4))
+        L = 16
+        h = OracleHarness(R, L, WIDTH, H, K, S_max, layers=2, lib=lib)
+        for c in range(calls):
+            B = int(rng.integers(1, R + 1))
+            S = int(rng.integers(1, S_max + 1))
+            layer = int(rng.integers(0, 2))
+            topk, rpi, sl = _random_call(rng, B, R, S, K, L)
+            h.call(topk, rpi, sl, layer=layer)
+
+
+def pin_simulator(lib, trials: int = 25, calls: int = 8) -> None:
+    rng = np.random.default_rng(19)
+    for trial in range(trials):
+        H = int(rng.integers(1, 9))
+        K = int(rng.integers(1, 9))
+        S_max = int(rng.integers(1, 5))
+        R = int(rng.integers(1, 4))
+        L = 16
+        h = OracleHarness(R, L, WIDTH, H, K, S_max, lib=lib)
+        sims = [ListCache(H, S_max * K) for _ in range(R)]
+        for c in range(calls):
+            B = int(rng.integers(1, R + 1))
+            S = int(rng.integers(1, S_max + 1))
+            topk, rpi, sl = _random_call(rng, B, R, S, K, L)
+            out = h.call(topk, rpi, sl, check=False)
+            for b in range(B):
+                q = int(rpi[b])
+                locs, stats = sims[q].call(q, topk[b].tolist(), min(int(sl[b]), L))
+                assert out["locs"][b].tolist() == locs, "locations differ from the list model"
+                assert out["stats"][b].tolist() == stats, "counters differ from the list model"
+                st = h.o.request_state(0, q)
+                assert st["tok"].tolist() == sims[q].tok
+                assert st["ep"].tolist() == sims[q].ep
+                assert st["phys"].tolist() == sims[q].phys
+                assert st["epoch"] == sims[q].epoch
+
+
+def pin_overflow(lib) -> None:
+    rng = np.random.default_rng(23)
+    seen_overflow = 0
+    for trial in range(30):
+        H = int(rng.integers(1, 6))
+        K = int(rng.integers(2, 9))
+        S = int(rng.integers(2, 5))
+        h = OracleHarness(2, 40, WIDTH, H, K, S, lib=lib)
+        for c in range(5):
+            topk = rng.integers(0, 40, size=(2, S, K)).astype(np.int32)
+            out = h.call(topk, np.array([0, 1], np.int32), np.array([40, 40], np.int32))
+            seen_overflow += int((out["stats"][:, 6] > 0).sum())
+    assert seen_overflow > 20
+
+
+def _steps_with_union(rng, S, K, union, universe):
+    """S distinct-per-step rows of K tokens whose union has exactly `union` tokens."""
+    assert K <= union <= S * K
+    pool = rng.permutation(universe)[:union]
+    steps = [pool[:K].copy()]
+    used = K
+    for s in range(1, S):
+        left = S - s  # steps still to fill, including this one
+        # spread the remaining new tokens evenly over the remaining steps
+        new = min(K, -(-(union - used) // left))
+        fresh = pool[used:used + new]
+        used += new
+        old = rng.choice(pool[:used - new], size=K - new, replace=False)
+        row = np.concatenate([fresh, old])
+        rng.shuffle(row)
+        steps.append(row)
+    assert used == union
+    return np.stack(steps).astype(np.int32)
+
+
+def pin_782(lib) -> None:
+    rng = np.random.default_rng(782)
+    S, K, H = 4, 256, 1024
+    h = OracleHarness(1, 4096, WIDTH, H, K, S, lib=lib)
+    topk = _steps_with_union(rng, S, K, 782, 4096)[None]
+    out = h.call(topk, np.array([0], np.int32), np.array([4096], np.int32))
+    st = out["stats"][0]
+    assert st[3] == 782 and st[2] == S * K - 782 and st[0] == 0
+    again = h.call(topk, np.array([0], np.int32), np.array([4096], np.int32))
+    assert again["stats"][0][0] == S * K and again["stats"][0][3] == 0
+
+
+def pin_page_table(lib) -> None:
+    from oracle import page_table
+    rng = np.random.default_rng(29)
+    for trial in range(30):
+        B, S, K = int(rng.integers(1, 4)), int(rng.integers(1, 5)), int(rng.integers(1, 40))
+        P = int(rng.integers(1, 20))
+        L = int(rng.integers(1, 300))
+        topk = rng.integers(-3, L + 5, size=(B, S, K)).astype(np.int32)
+        sl = rng.integers(1, L + 1, size=B).astype(np.int32)
+        pages, num, tp = page_table(topk, sl, P, lib=lib)
+        for b in range(B):
+            flat = topk[b].reshape(-1)
+            valid = (flat >= 0) & (flat < sl[b])
+            want = np.unique(flat[valid] // P)
+            assert num[b] == want.size
+            assert (pages[b, :want.size] == want).all() and (pages[b, want.size:] == -1).all()
+            idx = np.searchsorted(want, flat // P)
+            exp = np.where(valid, idx * P + flat % P, -1)
+            assert (tp[b].reshape(-1) == exp).all()
+
+
+ALL_PINS = (pin_lru, pin_first_call, pin_repeat_call, pin_invariants, pin_simulator,
+            pin_overflow, pin_782, pin_page_table)

@@ -1,0 +1,66 @@
+"""Plausible mistakes planted in a copy of the oracle must fail a pin.
+
+Each mutant is the oracle source with one textual change, compiled on the CPU
+into a temporary library.  The pins are run against it; the test passes only
+if at least one pin rejects the mutant.  The committed oracle is never
+modified.
+"""
+import os
+import tempfile
+
+import pytest
+
+import pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "oracle", "hs_oracle.cpp")
+
+MUTANTS = {
+    "mru_victims": ("if (rc.ep[a] != rc.ep[b]) return rc.ep[a] < rc.ep[b];",
+                    "if (rc.ep[a] != rc.ep[b]) return rc.ep[a] > rc.ep[b];"),
+    "highest_slot_tie_break": ("if (rc.ep[a] != rc.ep[b]) return rc.ep[a] < rc.ep[b];\n        return a < b;",
+                               "if (rc.ep[a] != rc.ep[b]) return rc.ep[a] < rc.ep[b];\n        return a > b;"),
+    "hits_not_marked": ("for (int32_t v : hit_slots) rc.ep[v] = E;", ""),
+    "oldest_step_preferred": ("return last_step[a] > last_step[b];",
+                              "return last_step[a] < last_step[b];"),
+    "last_step_not_updated": ("last_step[j] = s;\n                locs_b[i]",
+                              "locs_b[i]"),
+    "duplicate_at_wrong_row": ("locs_b[i] = (int32_t)(base + rc.phys[H + j]);",
+                               "locs_b[i] = (int32_t)(base + rc.phys[j]);"),
+    "off_by_one_validity": ("if (t < 0 || t >= limit)", "if (t < 0 || t > limit)"),
+    "copy_without_rotation": ("std::swap(rc.phys[v], rc.phys[H + j]);", ""),
+    "epoch_not_advanced": ("rc.epoch = E + 1;", "rc.epoch = E;"),
+    "cap_ignores_hits": ("const int32_t cap = H - (int32_t)hit_slots.size();",
+                         "const int32_t cap = H;"),
+    "victims_paired_unsorted": ("cand.resize(m);\n    std::sort(cand.begin(), cand.end());",
+                                "cand.resize(m);"),
+    "row_from_request_zero": ("const int64_t src_row = (int64_t)q * o.L + t;",
+                              "const int64_t src_row = t;"),
+    "seq_len_ignored": ("const int32_t limit = std::min(seq_len, o.L);",
+                        "const int32_t limit = o.L;"),
+    "evictions_not_counted": ("stat[HSO_STAT_EVICTED]++;", ""),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    from oracle.oracle import build_oracle, load_library
+    old, new = MUTANTS[name]
+    with open(ORACLE_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, "mutation anchor not found once: %r" % old
+    mutated = src.replace(old, new)
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "hs_oracle_mutant.cpp")
+        with open(path, "w") as f:
+            f.write(mutated)
+        lib_path = build_oracle(src=path, out_path=os.path.join(d, "libmutant.so"), force=True)
+        lib = load_library(lib_path)
+        caught = []
+        for pin in pins.ALL_PINS:
+            try:
+                pin(lib)
+            except AssertionError as e:
+                caught.append((pin.__name__, str(e)[:80]))
+                break
+        assert caught, "mutant %s passed every pin" % name
