@@ -288,15 +288,17 @@ int hso_reset_requests(hso_oracle* o, const int32_t* req_pool_indices, int32_t n
 // "SGLang HiSparse" sections 1.2 and 2.3 (PAGED mode: token -> page plus
 // in-page offset; only pages holding selected tokens reach attention).
 int hso_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t batch,
-                   int32_t num_steps, int32_t top_k, int32_t page_size, int32_t* pages,
-                   int32_t* num_pages, int32_t* token_page) {
-    if (batch < 0 || num_steps < 1 || top_k < 1 || page_size < 1) return HSO_ERR_ARG;
+                   int32_t num_steps, int32_t top_k, int32_t max_seq_len, int32_t page_size,
+                   int32_t* pages, int32_t* num_pages, int32_t* token_page) {
+    if (batch < 0 || num_steps < 1 || top_k < 1 || page_size < 1 || max_seq_len < 1)
+        return HSO_ERR_ARG;
     const int64_t n = (int64_t)num_steps * top_k;
     for (int32_t b = 0; b < batch; ++b) {
         const int32_t* t_b = topk + b * n;
+        const int32_t limit = std::min(seq_lens[b], max_seq_len);
         std::map<int32_t, int32_t> index;  // page -> position in the sorted list
         for (int64_t i = 0; i < n; ++i)
-            if (t_b[i] >= 0 && t_b[i] < seq_lens[b]) index[t_b[i] / page_size] = 0;
+            if (t_b[i] >= 0 && t_b[i] < limit) index[t_b[i] / page_size] = 0;
         int32_t p = 0;
         for (auto& kv : index) {
             pages[b * n + p] = kv.first;
@@ -306,7 +308,7 @@ int hso_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t batch,
         num_pages[b] = p;
         for (int64_t i = 0; i < n; ++i) {
             const int32_t t = t_b[i];
-            token_page[b * n + i] = (t >= 0 && t < seq_lens[b])
+            token_page[b * n + i] = (t >= 0 && t < limit)
                                         ? index[t / page_size] * page_size + t % page_size
                                         : -1;
         }

@@ -59,10 +59,11 @@ int hso_get_request_state(const hso_oracle* o, int32_t layer, int32_t q, int32_t
 /* Returns requests to the empty state in every layer. */
 int hso_reset_requests(hso_oracle* o, const int32_t* req_pool_indices, int32_t n);
 
-/* Sparse page table of one call (independent of the cache state). */
+/* Sparse page table of one call (independent of the cache state).  An entry
+ * is valid iff 0 <= t < min(seq_len, max_seq_len), as in hso_swap_in. */
 int hso_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t batch,
-                   int32_t num_steps, int32_t top_k, int32_t page_size, int32_t* pages,
-                   int32_t* num_pages, int32_t* token_page);
+                   int32_t num_steps, int32_t top_k, int32_t max_seq_len, int32_t page_size,
+                   int32_t* pages, int32_t* num_pages, int32_t* token_page);
 
 #ifdef __cplusplus
 }

@@ -65,7 +65,7 @@ def _declare(lib) -> None:
     lib.hso_reset_requests.argtypes = [ctypes.c_void_p, _i32p, ctypes.c_int32]
     lib.hso_page_table.restype = ctypes.c_int
     lib.hso_page_table.argtypes = [_i32p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                   ctypes.c_int32, _i32p, _i32p, _i32p]
+                                   ctypes.c_int32, ctypes.c_int32, _i32p, _i32p, _i32p]
 
 
 def load_library(path: Optional[str] = None):
@@ -163,7 +163,8 @@ class Oracle:
             raise ValueError("bad request index")
 
 
-def page_table(topk: np.ndarray, seq_lens: np.ndarray, page_size: int, lib=None):
+def page_table(topk: np.ndarray, seq_lens: np.ndarray, page_size: int,
+               max_seq_len: int = 2**31 - 1, lib=None):
     """Oracle sparse page table: (pages [B, S*K], num_pages [B], token_page [B, S, K])."""
     lib = lib if lib is not None else load_library()
     topk = np.ascontiguousarray(topk, dtype=np.int32)
@@ -172,7 +173,7 @@ def page_table(topk: np.ndarray, seq_lens: np.ndarray, page_size: int, lib=None)
     pages = np.empty((B, S * K), dtype=np.int32)
     num = np.empty(B, dtype=np.int32)
     tp = np.empty((B, S, K), dtype=np.int32)
-    rc = lib.hso_page_table(_ptr(topk, _i32p), _ptr(sl, _i32p), B, S, K, page_size,
+    rc = lib.hso_page_table(_ptr(topk, _i32p), _ptr(sl, _i32p), B, S, K, max_seq_len, page_size,
                             _ptr(pages, _i32p), _ptr(num, _i32p), _ptr(tp, _i32p))
     if rc != 0:
         raise ValueError("oracle page_table failed")

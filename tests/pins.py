@@ -206,11 +206,12 @@ def pin_page_table(lib) -> None:
         P = int(rng.integers(1, 20))
         L = int(rng.integers(1, 300))
         topk = rng.integers(-3, L + 5, size=(B, S, K)).astype(np.int32)
-        sl = rng.integers(1, L + 1, size=B).astype(np.int32)
-        pages, num, tp = page_table(topk, sl, P, lib=lib)
+        sl = rng.integers(1, L + 8, size=B).astype(np.int32)
+        L_max = int(rng.integers(1, L + 1))
+        pages, num, tp = page_table(topk, sl, P, max_seq_len=L_max, lib=lib)
         for b in range(B):
             flat = topk[b].reshape(-1)
-            valid = (flat >= 0) & (flat < sl[b])
+            valid = (flat >= 0) & (flat < min(sl[b], L_max))
             want = np.unique(flat[valid] // P)
             assert num[b] == want.size
             assert (pages[b, :want.size] == want).all() and (pages[b, want.size:] == -1).all()
