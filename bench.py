@@ -1,0 +1,429 @@
+"""Benchmark of the per-layer decode KV swap-in on one GB300 (or N replicas).
+
+One step is one layer-call of the whole hot path on one batch: gather
+(hash probe, cross-step miss dedup, locations), then commit (epoch-CLOCK
+victims, rotation, hash update) side by side with the miss-row copy from the
+pinned host pool, plus the sparse page table for the paged workload.
+
+Metric: selected tokens resolved per second per layer-call (B * S * K / step
+time).  Inputs (top-k, request slots, sequence lengths) are resident on the
+device before the timed region; L2 is flushed (a 256 MiB write) between timed
+steps.  Each timed step is bracketed by CUDA events on the launching stream.
+`e2e` repeats the measurement through the same C ABI calls with host buffers:
+per step the host->device copy of the inputs from pinned memory and the
+device->host read of the locations are inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C2]
+                       [--impl reference]
+Under torchrun each rank drives one GPU with its own copy of the workload
+(replicas, weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import hs_workloads as W  # noqa: E402
+
+METRIC = "selected tokens resolved/s per layer-call"
+UNIT = "tokens/s"
+PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--copy-ctas", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        used = inside
+        if not used and self.samples:  # region shorter than the sampling interval
+            mid = 0.5 * (t0 + t1)
+            used = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        out = {"samples_in_region": len(inside), "samples_used": len(used)}
+        if not used:
+            return out
+        try:
+            sm = [float(s[1]) for s in used]
+            out["sm_mhz"] = statistics.median(sm)
+            out["sm_max_mhz"] = max(float(s[2]) for s in used)
+            out["power_w_max"] = max(float(s[3]) for s in used)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            out["reasons"] = sorted({n for s in used for n, v in zip(names, s[5:9])
+                                     if v.lower().startswith("active")})
+        except (ValueError, IndexError):
+            out["raw"] = used[:3]
+        return out
+
+
+def measure_h2d_peak(torch, dev, nbytes=256 << 20, reps=20):
+    """Pinned host -> device cudaMemcpyAsync bandwidth, best of `reps` (GB/s)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    src.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = 0.0
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        s.record()
+        dst.copy_(src, non_blocking=True)
+        e.record()
+        e.synchronize()
+        best = max(best, nbytes / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def cpu_baseline_oracle(w, calls, rpi, sl, seconds, pool_np):
+    """The CPU oracle on the same stream: pre-roll untimed, then time calls
+    until `seconds` of CPU work (at least 2 calls)."""
+    from oracle import Oracle
+    threads = min(w.batch, os.cpu_count() or 1)
+    C = w.steps * w.top_k
+    o = Oracle(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, 1)
+    mirror = np.zeros((w.batch * (w.hot_buffer + C), w.row_bytes), dtype=np.uint8)
+    for c in calls[:PREROLL_CALLS]:
+        o.swap_in(0, pool_np, mirror, rpi, sl, c, num_threads=threads)
+    n = 0
+    t_total = 0.0
+    for c in calls[PREROLL_CALLS:]:
+        t = time.perf_counter()
+        o.swap_in(0, pool_np, mirror, rpi, sl, c, num_threads=threads)
+        t_total += time.perf_counter() - t
+        n += 1
+        if t_total >= seconds and n >= 2:
+            break
+    return {"value": w.entries * n / t_total, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d steady-state calls of %s after %d pre-roll calls (%d request threads, "
+                      "row copies included)" % (n, w.name, PREROLL_CALLS, threads)}
+
+
+def run_reference(args, w):
+    """--impl reference: the CPU oracle timed on this workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import Oracle
+    stream = W.TopkStream(w)
+    total_calls = PREROLL_CALLS + args.warmup + args.steps
+    calls = stream.calls(total_calls)
+    rpi, sl = W.req_pool_indices(w), W.seq_lens(w)
+    pool = np.empty((w.batch, w.seq_len, w.row_bytes), dtype=np.uint8)
+    W.fill_host_pool(pool, 0)
+    threads = min(w.batch, os.cpu_count() or 1)
+    C = w.steps * w.top_k
+    o = Oracle(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, 1)
+    mirror = np.zeros((w.batch * (w.hot_buffer + C), w.row_bytes), dtype=np.uint8)
+    for c in calls[:PREROLL_CALLS + args.warmup]:
+        o.swap_in(0, pool, mirror, rpi, sl, c, num_threads=threads)
+    times = []
+    for c in calls[PREROLL_CALLS + args.warmup:]:
+        t = time.perf_counter()
+        o.swap_in(0, pool, mirror, rpi, sl, c, num_threads=threads)
+        if w.page_size:
+            from oracle import page_table
+            page_table(c, sl, w.page_size, max_seq_len=w.seq_len)
+        times.append(time.perf_counter() - t)
+    ms = 1e3 * sum(times) / len(times)
+    value = w.entries / (ms * 1e-3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "impl": "reference",
+            "config": config_dict(w, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d timed calls of %s after %d pre-roll + %d warm-up calls"
+                                       % (args.steps, w.name, PREROLL_CALLS, args.warmup)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w, world):
+    return {"workload": "%s (%s)" % (w.name, "C%d" % w.cfg_id), "batch": w.batch,
+            "steps": w.steps, "top_k": w.top_k, "seq_len": w.seq_len, "hot_buffer": w.hot_buffer,
+            "row_bytes": w.row_bytes, "page_size": w.page_size, "index_mix": w.kind,
+            "reuse": w.reuse, "preroll_calls": PREROLL_CALLS,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": "replicas x%d" % world if world > 1 else "single GPU"}
+
+
+def main():
+    args = parse_args()
+    w = W.WORKLOADS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import sparse_attention_kv_swap_gb300 as pkg
+    from sparse_attention_kv_swap_gb300.cache import SwapInCache
+
+    K, Wm = args.steps, args.warmup
+    n_e2e = min(K, 20)
+    n_phase = min(K, 20)
+    total_calls = PREROLL_CALLS + Wm + K + n_phase + n_e2e
+    stream_gen = W.TopkStream(w)
+    calls = stream_gen.calls(total_calls)
+    rpi_np, sl_np = W.req_pool_indices(w), W.seq_lens(w)
+
+    cfg = pkg.make_config(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, 1)
+    pool = torch.empty((w.batch, w.seq_len, w.row_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_host_pool(pool.numpy(), 0)
+    cache = SwapInCache(cfg, host_pools=[pool], device=dev)
+    if args.copy_ctas:
+        pkg.hs_set_copy_ctas(cache.handle, args.copy_ctas)
+    s = torch.cuda.current_stream()
+
+    topk_all = torch.from_numpy(np.stack(calls)).to(dev)  # [calls, B, S, K]
+    rpi = torch.from_numpy(rpi_np).to(dev)
+    sl = torch.from_numpy(sl_np).to(dev)
+    Bn, S, Kk = w.batch, w.steps, w.top_k
+    locs = torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)
+    stats = torch.zeros((total_calls, Bn, pkg.binding.HS_NUM_STATS), dtype=torch.int32,
+                        device=dev)
+    page_out = None
+    if w.page_size:
+        page_out = {"pages": torch.empty((Bn, S * Kk), dtype=torch.int32, device=dev),
+                    "num_pages": torch.empty(Bn, dtype=torch.int32, device=dev),
+                    "token_page": torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(i, topk):
+        cache.swap_in(rpi, sl, topk, 0, out={"device_locs": locs, "stats": stats[i]})
+        if page_out is not None:
+            cache.page_table(topk, sl, w.page_size, out=page_out)
+
+    # pre-roll and warm-up
+    for i in range(PREROLL_CALLS + Wm):
+        step(i, topk_all[i])
+    torch.cuda.synchronize()
+    rc, flags = cache.status()
+    if flags:
+        raise RuntimeError("device status flags %#x after warm-up" % flags)
+
+    h2d_peak = measure_h2d_peak(torch, dev)
+    peaks = read_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_src = "MEASURED_PEAKS.json hbm_gbs (measured)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+
+    # ---- timed region: K steps, per-step events, L2 flush between steps ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.05)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    base = PREROLL_CALLS + Wm
+    for k in range(K):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(s)
+        step(base + k, topk_all[base + k])
+        ev[k][1].record(s)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.05)
+    clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / K
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = w.entries * world / (ms * 1e-3)
+    st_timed = stats[base:base + K].cpu().numpy()
+
+    # ---- phase split: gather vs commit + copy (separate pass, same stream) ----
+    e_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
+    e_m = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
+    e_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
+    pbase = base + K
+    for k in range(n_phase):
+        flush.fill_(k & 0xFF)
+        pkg.hs_set_phase_event(cache.handle, e_m[k])
+        e_a[k].record(s)
+        cache.swap_in(rpi, sl, topk_all[pbase + k], 0,
+                      out={"device_locs": locs, "stats": stats[pbase + k]})
+        e_b[k].record(s)
+    pkg.hs_set_phase_event(cache.handle, None)
+    torch.cuda.synchronize()
+    t_gather = [a.elapsed_time(m) for a, m in zip(e_a, e_m)]
+    t_cc = [m.elapsed_time(b) for m, b in zip(e_m, e_b)]
+    st_phase = stats[pbase:pbase + n_phase].cpu().numpy()
+
+    # ---- e2e: host buffers through the same C ABI call ----
+    ebase = pbase + n_phase
+    topk_host = torch.from_numpy(np.stack(calls[ebase:ebase + n_e2e])).pin_memory()
+    rpi_host = torch.from_numpy(rpi_np).pin_memory()
+    sl_host = torch.from_numpy(sl_np).pin_memory()
+    locs_host = torch.empty((Bn, S, Kk), dtype=torch.int32).pin_memory()
+    topk_dev = torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)
+    rpi_dev = torch.empty_like(rpi)
+    sl_dev = torch.empty_like(sl)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_e2e)]
+    torch.cuda.synchronize()
+    for k in range(n_e2e):
+        flush.fill_(k & 0xFF)
+        e2e_ev[k][0].record(s)
+        topk_dev.copy_(topk_host[k], non_blocking=True)
+        rpi_dev.copy_(rpi_host, non_blocking=True)
+        sl_dev.copy_(sl_host, non_blocking=True)
+        cache.swap_in(rpi_dev, sl_dev, topk_dev, 0, out={"device_locs": locs})
+        if page_out is not None:
+            cache.page_table(topk_dev, sl_dev, w.page_size, out=page_out)
+        locs_host.copy_(locs, non_blocking=True)
+        e2e_ev[k][1].record(s)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / n_e2e
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d_bytes = topk_host[0].numel() * 4 + rpi_host.numel() * 4 + sl_host.numel() * 4
+    d2h_bytes = locs_host.numel() * 4
+    rc, flags = cache.status()
+    if flags:
+        raise RuntimeError("device status flags %#x after the timed region" % flags)
+
+    # ---- roofline bookkeeping (algorithmic bytes) ----
+    U_phase = st_phase[:, :, 3].sum(axis=1).astype(np.float64)
+    m_phase = st_phase[:, :, 4].sum(axis=1).astype(np.float64)
+    hs_phase = st_phase[:, :, 1].sum(axis=1).astype(np.float64)
+    copy_bytes = U_phase * w.row_bytes  # host-link bytes (same again written to HBM)
+    cc_ms = np.asarray(t_cc)
+    g_ms = np.asarray(t_gather)
+    achieved_copy = float(np.mean(copy_bytes / (cc_ms * 1e-3)) / 1e9)
+    gather_bytes = 16.0 * w.entries + 16.0 * U_phase
+    commit_bytes = 8.0 * w.hot_buffer * w.batch + 32.0 * m_phase + 4.0 * hs_phase
+    achieved_gather = float(np.mean(gather_bytes / (g_ms * 1e-3)) / 1e9)
+    U_timed = st_timed[:, :, 3].sum(axis=1)
+
+    clk = clocks.summary(t_wall0, t_wall1)
+    n_kernels = 2 + (1 if page_out is not None else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": config_dict(w, world),
+        "e2e": {"value": w.entries * world / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
+                "ms_per_step": e2e_ms},
+        "gpu_launches": K * n_kernels,
+        "roofline": {"kernel": "commit_copy_kernel (commit CTAs + miss-row copy CTAs)",
+                     "bound": "host_link", "achieved": achieved_copy, "peak": h2d_peak,
+                     "unit": "GB/s", "frac": achieved_copy / h2d_peak, "traffic": None,
+                     "peak_source": "measured in this run: pinned host->device cudaMemcpyAsync "
+                                    "256 MiB, best of 20",
+                     "algorithmic_bytes_per_launch": float(np.mean(copy_bytes))},
+        "phases": {
+            "gather_ms": float(np.mean(g_ms)), "commit_copy_ms": float(np.mean(cc_ms)),
+            "gather_hbm": {"achieved": achieved_gather, "peak": hbm_peak, "unit": "GB/s",
+                           "frac": achieved_gather / hbm_peak, "peak_source": hbm_src,
+                           "algorithmic_bytes_per_launch": float(np.mean(gather_bytes))},
+            "commit_bytes_per_launch": float(np.mean(commit_bytes)),
+            "unique_misses_per_step": float(np.mean(U_timed)),
+            "miss_copy_mb_per_step": float(np.mean(U_timed)) * w.row_bytes / 1e6,
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        },
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_oracle(w, calls, rpi_np, sl_np, args.cpu_seconds,
+                                                   pool.numpy())
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

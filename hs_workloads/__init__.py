@@ -70,15 +70,54 @@ def host_rows(layer: int, q, t, width: int = ROW_BYTES) -> np.ndarray:
     return words.view(np.uint8).reshape(q.shape[0], width)
 
 
-def fill_host_pool(pool: np.ndarray, layer: int, chunk_rows: int = 1 << 16) -> None:
-    """Fill a host pool view uint8 [R, L, W] with rows (layer, q, t)."""
-    R, L, W = pool.shape
-    flat = pool.reshape(R * L, W)
-    total = R * L
-    for start in range(0, total, chunk_rows):
-        stop = min(total, start + chunk_rows)
+def _mix_inplace(z: np.ndarray) -> None:
+    """In-place SplitMix64 output function of counters z (uint64 array)."""
+    tmp = np.empty_like(z)
+    with np.errstate(over="ignore"):
+        z += np.uint64(1)
+        z *= _GAMMA
+        np.right_shift(z, np.uint64(30), out=tmp)
+        z ^= tmp
+        z *= _MIX1
+        np.right_shift(z, np.uint64(27), out=tmp)
+        z ^= tmp
+        z *= _MIX2
+        np.right_shift(z, np.uint64(31), out=tmp)
+        z ^= tmp
+
+
+def fill_host_pool(pool: np.ndarray, layer: int, chunk_rows: int = 1 << 14,
+                   threads: Optional[int] = None) -> None:
+    """Fill a host pool view uint8 [R, L, W] with rows (layer, q, t).
+
+    Same bytes as host_rows(); written in place, chunk by chunk, on a few
+    threads (numpy releases the GIL inside its loops).
+    """
+    import concurrent.futures as cf
+    import os
+
+    R, L, Wd = pool.shape
+    assert Wd % 8 == 0 and pool.flags["C_CONTIGUOUS"]
+    nw = Wd // 8
+    words = pool.reshape(R * L, Wd).view(np.uint64)
+    offs = np.arange(nw, dtype=np.uint64)[None, :]
+
+    def fill(start: int) -> None:
+        stop = min(R * L, start + chunk_rows)
         idx = np.arange(start, stop, dtype=np.int64)
-        flat[start:stop] = host_rows(layer, idx // L, idx % L, W)
+        base = row_counter(layer, idx // L, idx % L)[:, None]
+        z = words[start:stop]
+        np.add(base, offs, out=z)
+        _mix_inplace(z)
+
+    starts = range(0, R * L, chunk_rows)
+    n = threads or min(16, os.cpu_count() or 1)
+    if n <= 1 or len(starts) == 1:
+        for st in starts:
+            fill(st)
+        return
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(fill, starts))
 
 
 @dataclasses.dataclass(frozen=True)

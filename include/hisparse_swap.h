@@ -1,0 +1,225 @@
+/*
+ * hisparse_swap.h -- C ABI of the GB300 decode KV swap-in library.
+ *
+ * The library resolves, for each decode step and layer, every request's
+ * indexer top-k token indices against a per-request device hot buffer that
+ * is backed by a pinned host KV pool, and returns the device row of every
+ * selected token (plus, on request, a sparse page table).  One call:
+ *   1. looks each token up in the request's token -> slot hash,
+ *   2. de-duplicates misses within and across the speculative steps,
+ *   3. copies each unique miss's KV row from mapped pinned host memory into a
+ *      scratch row of the device buffer,
+ *   4. commits: marks the referenced hot slots, evicts the least recently
+ *      referenced slots (epoch-CLOCK), rotates the scratch rows into the
+ *      victims' hot slots and updates the hash.
+ * Sources: "[HiSparse] Support hisparse multi-step swap io kernel" (PR
+ * #32162 report), sections 功能与动机, 实现拆解 item 1-2, 关键源码片段
+ * (HiSparseSpecState) and 风险与影响; PR #20343 summary, 实现拆解
+ * (swap_in_selected_pages, device/host mapped pool); "SGLang HiSparse:
+ * 当稀疏注意力从算法变为系统组件", sections 2.1 and 2.3.
+ *
+ * Conventions for every call:
+ *  - Pointers named *_dev are device pointers; *_host are host pointers.
+ *    The caller owns every buffer (pinned host pool, device KV buffers,
+ *    state, workspace, inputs, outputs).  The library owns only the small
+ *    host handle `hs_state`.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on that stream unless stated.  Calls
+ *    that share one hs_state must be ordered on one stream (or by events):
+ *    they share the state and the workspace.
+ *  - Return value: HS_OK (0) or a negative HS_ERR_* code; nothing aborts or
+ *    throws.  Argument errors are detected on the host before any launch.
+ *    Data-dependent problems found by the kernels (request index out of
+ *    range, a request twice in one call, seq_len above max_seq_len, hash
+ *    probe limit) set bits in a device status word read by hs_get_status.
+ *  - Token index t of batch row b is valid iff 0 <= t < min(seq_lens[b],
+ *    max_seq_len); invalid entries get location -1 and change nothing.
+ *  - Layouts (row-major, densest index last):
+ *      host pool of layer l      uint8 [R, max_seq_len, W], row (q, t)
+ *      device KV buffer of layer uint8 [R, H + C, W], C = max_steps * top_k
+ *      top-k indices             int32 [B, S, top_k]
+ *      device_locs               int32 [B, S, top_k]: row index into the
+ *                                layer's device KV buffer (q * (H + C) + p)
+ */
+#ifndef HISPARSE_SWAP_H
+#define HISPARSE_SWAP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define HS_OK 0
+#define HS_ERR_INVALID_ARG (-1)   /* bad pointer, size, index or config      */
+#define HS_ERR_UNSUPPORTED (-2)   /* valid but beyond this build's limits    */
+#define HS_ERR_CUDA (-3)          /* a CUDA runtime call or launch failed    */
+#define HS_ERR_DEVICE_STATUS (-4) /* hs_get_status found device flags set    */
+#define HS_ERR_TIMEOUT (-5)       /* a bounded device wait gave up           */
+
+/* ---- device status flags (hs_get_status) -------------------------------- */
+#define HS_STATUS_BAD_REQUEST 0x1u       /* req_pool_indices[b] outside [0, R) */
+#define HS_STATUS_DUPLICATE_REQUEST 0x2u /* a request twice in one call        */
+#define HS_STATUS_SEQ_LEN_CLAMPED 0x4u   /* seq_lens[b] > max_seq_len          */
+#define HS_STATUS_PROBE_LIMIT 0x8u       /* hash probe exceeded the table      */
+#define HS_STATUS_TABLE_FULL 0x10u       /* hash insert found no free entry    */
+
+/* ---- per-request counters of one call (int32 [B, HS_NUM_STATS]) -------- */
+#define HS_STAT_HITS 0          /* valid entries whose token was resident   */
+#define HS_STAT_HIT_SLOTS 1     /* distinct hot slots those hits referenced */
+#define HS_STAT_DUP_MISSES 2    /* miss entries repeating an earlier miss   */
+#define HS_STAT_UNIQUE_MISSES 3 /* U: distinct non-resident valid tokens    */
+#define HS_STAT_ADMITTED 4      /* m = min(U, H - hit slots)                */
+#define HS_STAT_EVICTED 5       /* admitted into a slot that held a token   */
+#define HS_STAT_OVERFLOW 6      /* U - m: served this call, not admitted    */
+#define HS_STAT_INVALID 7       /* entries outside [0, min(seq_len, L_max)) */
+#define HS_NUM_STATS 8
+
+/* Limits of this build. */
+#define HS_MAX_HOT_BUFFER 32768  /* hot_buffer_size upper bound (PR #32162 report, 风险与影响) */
+#define HS_MAX_STEPS 4           /* speculative steps per call (same report, 实现拆解 item 2) */
+#define HS_MAX_ENTRIES 8192      /* max_steps * top_k per request per call */
+#define HS_MAX_PAGES 262144      /* ceil(max_seq_len / page_size) for hs_page_table */
+
+typedef struct hs_config {
+    int32_t num_requests;    /* R: request-pool slots (req_pool_indices range)    */
+    int32_t max_seq_len;     /* L_max: host rows per request and layer            */
+    int32_t item_size_bytes; /* W: bytes per KV row; a multiple of 16 (656 = MLA) */
+    int32_t hot_buffer_size; /* H: hot slots per request and layer, 1..32768      */
+    int32_t top_k;           /* K: indices per request and step                   */
+    int32_t max_steps;       /* S_max: 1..4 speculative steps                     */
+    int32_t num_layers;      /* layers sharing one state object                   */
+    int32_t max_batch;       /* B_max: requests per call, <= num_requests         */
+} hs_config;
+
+typedef struct hs_state hs_state; /* opaque host handle */
+
+/* Returns HS_OK if `cfg` is valid and supported, else the error code.
+ * Host only; no CUDA call. */
+int hs_config_check(const hs_config* cfg);
+
+/* Sizes the caller must allocate (0 if the config is not accepted).
+ * Host only; no CUDA call.
+ *   state:      device bytes, persistent cache state of all layers
+ *               (hash banks, slot epochs, slot tokens, position table,
+ *               control words)
+ *   workspace:  device bytes, per-call scratch shared by all layers
+ *   device_kv:  device bytes of ONE layer's KV buffer, R * (H + C) * W
+ *   host_pool:  pinned host bytes of ONE layer's pool, R * L_max * W
+ * `hash_size` is the entries of one request's hash bank (power of two). */
+size_t hs_state_bytes(const hs_config* cfg);
+size_t hs_workspace_bytes(const hs_config* cfg);
+size_t hs_device_kv_bytes(const hs_config* cfg);
+size_t hs_host_pool_bytes(const hs_config* cfg);
+int32_t hs_hash_size(const hs_config* cfg);
+
+/* Creates the host handle and initialises the state on `stream`: every
+ * request empty, no token resident, position table the identity, epoch 0.
+ *   host_pool_host[l]: host pool of layer l, 16-byte aligned.  Pinned memory
+ *     (cudaHostAlloc'd or cudaHostRegister'ed) is used through its device
+ *     mapping (cudaHostGetDevicePointer).  Plain pageable memory is accepted
+ *     only on devices that read host page tables directly
+ *     (cudaDevAttrPageableMemoryAccess, e.g. Grace NVLink-C2C systems);
+ *     elsewhere it fails with HS_ERR_INVALID_ARG.
+ *   device_kv_dev[l]: device KV buffer of layer l, 16-byte aligned.
+ *   state_dev / workspace_dev: 256-byte aligned device memory of at least
+ *     hs_state_bytes / hs_workspace_bytes.
+ * The pointer arrays are copied; the memory they point to must outlive the
+ * handle.  Synchronous with respect to the host only for the pointer
+ * queries; the initialisation kernel runs on `stream`. */
+int hs_create_state(const hs_config* cfg, void* const* host_pool_host,
+                    void* const* device_kv_dev, void* state_dev, size_t state_bytes,
+                    void* workspace_dev, size_t workspace_bytes, void* stream,
+                    hs_state** out);
+
+/* Frees the host handle only (never the caller's memory). NULL is a no-op. */
+void hs_destroy_state(hs_state* st);
+
+/* One per-layer swap-in call (the page's swap_in_selected_pages(
+ * req_pool_indices, seq_lens, topk_indices, layer_id)).
+ *   req_pool_indices_dev int32 [batch]: distinct request slots in [0, R)
+ *   seq_lens_dev         int32 [batch]
+ *   topk_dev             int32 [batch, num_steps, top_k]
+ *   batch                0..max_batch (0 is a no-op)
+ *   num_steps            1..max_steps (1 = single-step decode)
+ *   device_locs_dev      int32 [batch, num_steps, top_k] out
+ *   stats_dev            int32 [batch, HS_NUM_STATS] out, or NULL
+ *   miss_src_dev         int64 [batch, C] out or NULL: host row
+ *                        (q * max_seq_len + t) of unique miss j
+ *   miss_dst_dev         int64 [batch, C] out or NULL: device row it was
+ *                        copied to (the location returned for it)
+ *   miss_count_dev       int32 [batch] out or NULL: unique misses U
+ *   (the three miss-plan pointers are all NULL or all non-NULL; entries
+ *    j >= U are left untouched)
+ * Locations stay valid until the next call on the same layer.  Launches two
+ * kernels on `stream`; the second uses programmatic dependent launch. */
+int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t* seq_lens_dev,
+               const int32_t* topk_dev, int32_t batch, int32_t num_steps, int32_t layer_id,
+               int32_t* device_locs_dev, int32_t* stats_dev, int64_t* miss_src_dev,
+               int64_t* miss_dst_dev, int32_t* miss_count_dev, void* stream);
+
+/* Sparse page table of one call (PAGED mode: token -> page + in-page
+ * offset; only pages holding selected tokens; "SGLang HiSparse" sections
+ * 1.2, 2.1 and 2.3).  Stateless.  For batch row b:
+ *   pages_dev      int32 [batch, num_steps * top_k]: the distinct pages
+ *                  t / page_size of b's valid tokens, ascending, then -1
+ *   num_pages_dev  int32 [batch]
+ *   token_page_dev int32 [batch, num_steps, top_k]: for a valid token,
+ *                  (index of its page in pages[b]) * page_size +
+ *                  t % page_size; -1 for an invalid one.
+ * Validity as in hs_swap_in with L_max = max_seq_len.  Requires
+ * ceil(max_seq_len / page_size) <= HS_MAX_PAGES and num_steps * top_k <=
+ * HS_MAX_ENTRIES. */
+int hs_page_table(const int32_t* topk_dev, const int32_t* seq_lens_dev, int32_t batch,
+                  int32_t num_steps, int32_t top_k, int32_t max_seq_len, int32_t page_size,
+                  int32_t* pages_dev, int32_t* num_pages_dev, int32_t* token_page_dev,
+                  void* stream);
+
+/* Returns requests to the empty state in every layer (use when a request
+ * slot is given to a new sequence; order it after the previous user's last
+ * call and before the new user's first call on `stream`). */
+int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t n,
+                      void* stream);
+
+/* Synchronises `stream`, returns the device status flags (HS_STATUS_*) in
+ * *flags_out and clears them.  Returns HS_ERR_DEVICE_STATUS if any flag was
+ * set, HS_OK otherwise. */
+int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream);
+
+/* Copies one request's policy state of one layer to host memory and
+ * synchronises `stream` (checkpointing and tests).  Any output may be NULL.
+ *   tok_host  int32 [H]: token held by each hot slot, -1 if empty
+ *   ep_host   int32 [H]: epoch of the slot's last reference, -1 if never
+ *   phys_host int32 [H + C]: physical row of each position (a permutation)
+ *   ctrl_host int32 [8]: {next epoch, resident count, used hash entries, ...}
+ *   bank_host int64 [hash_size]: hash entries (t << 32 | slot), -1 empty,
+ *             -2 deleted */
+int hs_export_request_state(hs_state* st, int32_t layer_id, int32_t request, int32_t* tok_host,
+                            int32_t* ep_host, int32_t* phys_host, int32_t* ctrl_host,
+                            int64_t* bank_host, void* stream);
+
+/* Profiling: when `event_host` (a cudaEvent_t) is non-NULL, every later
+ * hs_swap_in on this handle records it on its stream between the gather
+ * kernel and the commit + copy kernel, and launches the latter without
+ * programmatic dependent launch, so that a caller can time the two kernels
+ * separately with its own events.  NULL restores the default.  Host only. */
+int hs_set_phase_event(hs_state* st, void* event_host);
+
+/* Tuning: CTAs of the commit + copy kernel that copy miss rows (in addition
+ * to one commit CTA per batch row).  0 restores the default (twice the SM
+ * count); otherwise 1..65535.  Host only. */
+int hs_set_copy_ctas(hs_state* st, int32_t copy_ctas);
+
+/* Static string for a return code. */
+const char* hs_status_string(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t hs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HISPARSE_SWAP_H */

@@ -1,0 +1,304 @@
+"""Thin ctypes binding of the C ABI in include/hisparse_swap.h.
+
+Every function here only marshals arguments (tensor pointers, sizes, the
+current CUDA stream) and calls the library of the same name; all work runs
+in the library's CUDA kernels.  There is no fallback: if the library has not
+been built for this machine, loading it raises.
+
+Tensors: device tensors are torch CUDA tensors, host pools are pinned torch
+CPU tensors (``pin_memory=True``); all must be contiguous.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Dict, List, Optional, Sequence
+
+from . import build as _build
+
+HS_OK = 0
+HS_ERR_INVALID_ARG = -1
+HS_ERR_UNSUPPORTED = -2
+HS_ERR_CUDA = -3
+HS_ERR_DEVICE_STATUS = -4
+HS_ERR_TIMEOUT = -5
+
+HS_STATUS_BAD_REQUEST = 0x1
+HS_STATUS_DUPLICATE_REQUEST = 0x2
+HS_STATUS_SEQ_LEN_CLAMPED = 0x4
+HS_STATUS_PROBE_LIMIT = 0x8
+HS_STATUS_TABLE_FULL = 0x10
+
+HS_NUM_STATS = 8
+STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "evicted",
+              "overflow", "invalid")
+
+HEADER = os.path.join(_build.INCLUDE, "hisparse_swap.h")
+
+
+class HsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, status_string(code), code))
+
+
+class HsConfig(ctypes.Structure):
+    _fields_ = [("num_requests", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("item_size_bytes", ctypes.c_int32), ("hot_buffer_size", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("max_steps", ctypes.c_int32),
+                ("num_layers", ctypes.c_int32), ("max_batch", ctypes.c_int32)]
+
+    def as_dict(self) -> Dict[str, int]:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+def make_config(num_requests: int, max_seq_len: int, item_size_bytes: int,
+                hot_buffer_size: int, top_k: int, max_steps: int, num_layers: int = 1,
+                max_batch: Optional[int] = None) -> HsConfig:
+    return HsConfig(num_requests, max_seq_len, item_size_bytes, hot_buffer_size, top_k,
+                    max_steps, num_layers, num_requests if max_batch is None else max_batch)
+
+
+_lib = None
+_lock = threading.Lock()
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_cfgp = ctypes.POINTER(HsConfig)
+
+
+def _declare(lib) -> None:
+    sig = {
+        "hs_config_check": (ctypes.c_int, [_cfgp]),
+        "hs_state_bytes": (ctypes.c_size_t, [_cfgp]),
+        "hs_workspace_bytes": (ctypes.c_size_t, [_cfgp]),
+        "hs_device_kv_bytes": (ctypes.c_size_t, [_cfgp]),
+        "hs_host_pool_bytes": (ctypes.c_size_t, [_cfgp]),
+        "hs_hash_size": (_i32, [_cfgp]),
+        "hs_create_state": (ctypes.c_int, [_cfgp, _vp, _vp, _vp, ctypes.c_size_t, _vp,
+                                           ctypes.c_size_t, _vp, ctypes.POINTER(_vp)]),
+        "hs_destroy_state": (None, [_vp]),
+        "hs_swap_in": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                      _vp, _vp]),
+        "hs_page_table": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                         _vp]),
+        "hs_reset_requests": (ctypes.c_int, [_vp, _vp, _i32, _vp]),
+        "hs_get_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+        "hs_export_request_state": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                                   _vp]),
+        "hs_set_phase_event": (ctypes.c_int, [_vp, _vp]),
+        "hs_set_copy_ctas": (ctypes.c_int, [_vp, _i32]),
+        "hs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "hs_version": (_i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+
+
+def load_library(path: Optional[str] = None, build_if_missing: bool = False):
+    """Load the in-tree library (optionally building it first)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.lib_path()
+        if not os.path.exists(p):
+            if not build_if_missing:
+                raise RuntimeError("CUDA library %s is not built; run __graft_entry__.build() or "
+                                   "python -m sparse_attention_kv_swap_gb300.build" % p)
+            p = _build.build()
+        lib = ctypes.CDLL(p)
+        _declare(lib)
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def header_symbols(header: str = HEADER) -> List[str]:
+    """Names of the functions the public header declares."""
+    with open(header) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hs_[a-z_0-9]+)\s*\(", text)))
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().hs_status_string(code).decode()
+    except Exception:
+        return "status %d" % code
+
+
+def _check(code: int, where: str) -> None:
+    if code != HS_OK:
+        raise HsError(code, where)
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dptr(t, dtype=None, name="tensor") -> int:
+    if t is None:
+        return 0
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must have dtype %s" % (name, dtype))
+    return int(t.data_ptr())
+
+
+# ---- sizes -----------------------------------------------------------------
+
+def hs_config_check(cfg: HsConfig) -> int:
+    return load_library().hs_config_check(ctypes.byref(cfg))
+
+
+def hs_state_bytes(cfg: HsConfig) -> int:
+    return load_library().hs_state_bytes(ctypes.byref(cfg))
+
+
+def hs_workspace_bytes(cfg: HsConfig) -> int:
+    return load_library().hs_workspace_bytes(ctypes.byref(cfg))
+
+
+def hs_device_kv_bytes(cfg: HsConfig) -> int:
+    return load_library().hs_device_kv_bytes(ctypes.byref(cfg))
+
+
+def hs_host_pool_bytes(cfg: HsConfig) -> int:
+    return load_library().hs_host_pool_bytes(ctypes.byref(cfg))
+
+
+def hs_hash_size(cfg: HsConfig) -> int:
+    return load_library().hs_hash_size(ctypes.byref(cfg))
+
+
+def hs_version() -> int:
+    return load_library().hs_version()
+
+
+def hs_status_string(code: int) -> str:
+    return load_library().hs_status_string(code).decode()
+
+
+# ---- state -------------------------------------------------------------------
+
+class StateHandle:
+    """Owns the library's host handle; keeps the caller's tensors alive."""
+
+    def __init__(self, ptr: int, cfg: HsConfig, keep: Sequence):
+        self.ptr = ctypes.c_void_p(ptr)
+        self.cfg = cfg
+        self._keep = list(keep)
+
+    def close(self) -> None:
+        if self.ptr:
+            load_library().hs_destroy_state(self.ptr)
+            self.ptr = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def hs_create_state(cfg: HsConfig, host_pools: Sequence, device_kvs: Sequence, state, workspace,
+                    stream=None) -> StateHandle:
+    lib = load_library()
+    L = cfg.num_layers
+    if len(host_pools) != L or len(device_kvs) != L:
+        raise ValueError("need one host pool and one device KV buffer per layer")
+    hp = (ctypes.c_void_p * L)(*[_dptr(t, name="host pool") for t in host_pools])
+    dk = (ctypes.c_void_p * L)(*[_dptr(t, name="device kv") for t in device_kvs])
+    out = ctypes.c_void_p()
+    rc = lib.hs_create_state(ctypes.byref(cfg), ctypes.cast(hp, _vp), ctypes.cast(dk, _vp),
+                             _dptr(state, name="state"), state.numel() * state.element_size(),
+                             _dptr(workspace, name="workspace"),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream),
+                             ctypes.byref(out))
+    _check(rc, "hs_create_state")
+    return StateHandle(out.value, cfg, list(host_pools) + list(device_kvs) + [state, workspace])
+
+
+def hs_destroy_state(handle: StateHandle) -> None:
+    handle.close()
+
+
+def hs_swap_in(handle: StateHandle, req_pool_indices, seq_lens, topk, layer_id: int,
+               device_locs, stats=None, miss_src=None, miss_dst=None, miss_count=None,
+               stream=None) -> None:
+    import torch
+    B, S, K = topk.shape
+    rc = load_library().hs_swap_in(
+        handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
+        _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
+        layer_id, _dptr(device_locs, torch.int32, "device_locs"),
+        _dptr(stats, torch.int32, "stats"), _dptr(miss_src, torch.int64, "miss_src"),
+        _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
+        _stream_ptr(stream))
+    _check(rc, "hs_swap_in")
+
+
+def hs_page_table(topk, seq_lens, max_seq_len: int, page_size: int, pages, num_pages,
+                  token_page, stream=None) -> None:
+    import torch
+    B, S, K = topk.shape
+    rc = load_library().hs_page_table(
+        _dptr(topk, torch.int32, "topk"), _dptr(seq_lens, torch.int32, "seq_lens"), B, S, K,
+        max_seq_len, page_size, _dptr(pages, torch.int32, "pages"),
+        _dptr(num_pages, torch.int32, "num_pages"), _dptr(token_page, torch.int32, "token_page"),
+        _stream_ptr(stream))
+    _check(rc, "hs_page_table")
+
+
+def hs_reset_requests(handle: StateHandle, req_pool_indices, stream=None) -> None:
+    import torch
+    rc = load_library().hs_reset_requests(
+        handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
+        req_pool_indices.numel(), _stream_ptr(stream))
+    _check(rc, "hs_reset_requests")
+
+
+def hs_get_status(handle: StateHandle, stream=None):
+    """Returns (code, flags); synchronises the stream and clears the flags."""
+    flags = ctypes.c_uint32(0)
+    rc = load_library().hs_get_status(handle.ptr, ctypes.byref(flags), _stream_ptr(stream))
+    if rc not in (HS_OK, HS_ERR_DEVICE_STATUS):
+        _check(rc, "hs_get_status")
+    return rc, flags.value
+
+
+def hs_export_request_state(handle: StateHandle, layer_id: int, request: int, stream=None):
+    import numpy as np
+    cfg = handle.cfg
+    H = cfg.hot_buffer_size
+    C = cfg.max_steps * cfg.top_k
+    tok = np.empty(H, np.int32)
+    ep = np.empty(H, np.int32)
+    phys = np.empty(H + C, np.int32)
+    ctrl = np.empty(8, np.int32)
+    bank = np.empty(hs_hash_size(cfg), np.int64)
+    rc = load_library().hs_export_request_state(
+        handle.ptr, layer_id, request, tok.ctypes.data, ep.ctypes.data, phys.ctypes.data,
+        ctrl.ctypes.data, bank.ctypes.data, _stream_ptr(stream))
+    _check(rc, "hs_export_request_state")
+    return {"tok": tok, "ep": ep, "phys": phys, "ctrl": ctrl, "bank": bank,
+            "epoch": int(ctrl[0])}
+
+
+def hs_set_phase_event(handle: StateHandle, event=None) -> None:
+    """event: a torch.cuda.Event (created with enable_timing) or None."""
+    ptr = 0 if event is None else int(event.cuda_event)
+    _check(load_library().hs_set_phase_event(handle.ptr, ptr), "hs_set_phase_event")
+
+
+def hs_set_copy_ctas(handle: StateHandle, copy_ctas: int) -> None:
+    _check(load_library().hs_set_copy_ctas(handle.ptr, copy_ctas), "hs_set_copy_ctas")

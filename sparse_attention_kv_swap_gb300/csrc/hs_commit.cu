@@ -1,0 +1,407 @@
+// Commit + copy kernel of the decode KV swap-in (sm_103a).
+//
+// Launched right behind the gather kernel with programmatic dependent
+// launch; every CTA first waits for the gather grid's results.  The grid has
+// two kinds of CTA that run side by side:
+//
+//  * CTAs 0..B-1 commit one request each (the multi-step swap report,
+//    section 实现拆解 item 1: CLOCK update, rotation of scratch and hot
+//    locations, token -> slot hash update, resolution of overflowing misses;
+//    section 风险与影响: overflow admission prefers the latest step):
+//      - hot slots referenced by the call already carry its epoch E (the
+//        gather stamped them), so cap = H - #{ep == E} and m = min(U, cap);
+//      - victims: the m non-hit slots with the smallest (epoch, slot); a
+//        radix select over epoch + 1 finds the threshold epoch and how many
+//        slots at the threshold to take (the lowest ones);
+//      - admitted misses: all if U <= cap, otherwise the m best by (last step
+//        descending, ordinal ascending);
+//      - the i-th admitted miss (ascending ordinal) takes the i-th victim
+//        (ascending slot): its old token leaves the hash, phys[v] and
+//        phys[H + j] swap (the copied row becomes the hot row, no second
+//        copy), the new token enters the hash and the slot takes epoch E.
+//  * the other CTAs copy every unique miss's KV row from the mapped pinned
+//    host pool to the device row the gather returned for it: 16-byte
+//    vectors, consecutive threads on consecutive 16-byte pieces of a row,
+//    all of a thread's loads issued before its stores.
+// The two never touch the same memory: the copy reads the miss lists and
+// writes device KV rows, the commit rewrites only the policy state.
+#include "hs_internal.cuh"
+
+namespace hs {
+namespace {
+
+constexpr int kBlock = 512;
+constexpr int kCopyUnroll = 6;
+constexpr unsigned kHitKey = 0xffffffffu;  // radix key of a slot referenced by the call
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, const uint4& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Deletes token t from a request's hash bank (the entry must exist).
+__device__ void bank_delete(long long* bank, int shift, unsigned mask, int32_t t,
+                            uint32_t* status) {
+    unsigned p = hash_token(t, shift);
+    for (unsigned n = 0; n <= mask; ++n) {
+        const long long x = bank[p];
+        if (x == kEmpty) break;
+        if (x >= 0 && (int)(x >> 32) == t) {
+            bank[p] = kDeleted;
+            return;
+        }
+        p = (p + 1u) & mask;
+    }
+    atomicOr(status, HS_STATUS_PROBE_LIMIT);
+}
+
+// Inserts (t, slot) at the first empty or deleted entry of t's probe
+// sequence; returns 1 if the entry was never used before.
+__device__ int bank_insert(long long* bank, int shift, unsigned mask, int32_t t, int32_t slot,
+                           uint32_t* status) {
+    const long long e = make_entry(t, slot);
+    unsigned p = hash_token(t, shift);
+    for (unsigned n = 0; n <= mask; ++n) {
+        long long x = bank[p];
+        while (x < 0) {
+            const long long y = atomicCAS(reinterpret_cast<unsigned long long*>(&bank[p]),
+                                          (unsigned long long)x, (unsigned long long)e);
+            if (y == x) return x == kEmpty ? 1 : 0;
+            x = y;
+        }
+        p = (p + 1u) & mask;
+    }
+    atomicOr(status, HS_STATUS_TABLE_FULL);
+    return 0;
+}
+
+// Finds the `need`-th smallest key (1-based) among keys[0..n) that are not
+// kHitKey, by most-significant-digit radix select over `bits` bits.
+// Returns the key; *need_out is how many keys equal to it to take.
+__device__ unsigned radix_select(const unsigned* keys, int n, int need, int bits, int* hist,
+                                 int* sh, int* need_out) {
+    unsigned prefix = 0u;
+    int top = ((bits + 7) / 8) * 8;
+    for (int shift = top - 8; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        for (int v = threadIdx.x; v < n; v += blockDim.x) {
+            const unsigned k = keys[v];
+            if (k == kHitKey) continue;
+            if (shift + 8 < 32 && (k >> (shift + 8)) != prefix) continue;
+            atomicAdd(&hist[(k >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            int c[8];
+            int sum = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                c[k] = hist[lane * 8 + k];
+                sum += c[k];
+            }
+            const int inc = warp_inclusive_scan(sum);
+            const int exc = inc - sum;
+            const bool here = exc < need && need <= inc;
+            if (here) {
+                int run = exc;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (run < need && need <= run + c[k]) {
+                        sh[0] = lane * 8 + k;
+                        sh[1] = need - run;
+                    }
+                    run += c[k];
+                }
+            }
+        }
+        __syncthreads();
+        prefix = (prefix << 8) | (unsigned)sh[0];
+        need = sh[1];
+        __syncthreads();
+    }
+    *need_out = need;
+    return prefix;
+}
+
+__device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
+    __shared__ int s_tmp[33];
+    __shared__ int s_hist[256];
+    __shared__ int s_sel[2];
+    __shared__ int s_misc[8];
+
+    const Dims& d = a.d;
+    const int32_t* cnt = a.ws.cnt + (long long)b * kCntWords;
+    if (cnt[CNT_SKIP]) return;
+    const int tid = threadIdx.x, BD = blockDim.x;
+    const int q = cnt[CNT_Q];
+    const int U = cnt[CNT_U];
+    const int H = d.H;
+    int32_t* ctrl = a.lv.ctrl + (long long)q * kCtrlWords;
+    const int E = ctrl[CTRL_EPOCH];
+    int32_t* ep = a.lv.ep + (long long)q * H;
+    int32_t* tok = a.lv.tok + (long long)q * H;
+    int32_t* phys = a.lv.phys + (long long)q * (H + d.C);
+    long long* bank = a.lv.bank + (long long)q * d.hash_size;
+    const unsigned hmask = (unsigned)d.hash_size - 1u;
+    const long long wbase = (long long)b * d.C;
+    int32_t* vict = a.ws.vict + wbase;
+    int32_t* adm = a.ws.adm + wbase;
+
+    // Keys for victim selection: epoch + 1 (0 = never used), or kHitKey.
+    int nhit = 0;
+    for (int v = tid; v < H; v += BD) {
+        const int e = ep[v];
+        const bool hit = (e == E);
+        keys[v] = hit ? kHitKey : (unsigned)(e + 1);
+        nhit += hit;
+    }
+    nhit = block_sum(nhit, s_tmp);  // includes the barrier that publishes keys
+    const int cap = H - nhit;
+    const int m = U < cap ? U : cap;
+
+    int evicted = 0;
+    if (m > 0) {
+        // ---- victims: m smallest (key, slot) among non-hit slots ------------
+        const int bits = 32 - __clz(E);  // keys lie in [0, E]
+        int need = m;
+        unsigned thr = 0u;
+        if (bits > 0) thr = radix_select(keys, H, m, bits, s_hist, s_sel, &need);
+        // Thread-contiguous segments keep slot order for the scans.
+        const int seg = (H + BD - 1) / BD;
+        const int v0 = tid * seg, v1 = min(H, v0 + seg);
+        int eq = 0;
+        for (int v = v0; v < v1; ++v) eq += (keys[v] == thr);
+        int eq_total;
+        int eq_before = block_exclusive_scan(eq, s_tmp, &eq_total);
+        int nv = 0;
+        {
+            int er = eq_before;
+            for (int v = v0; v < v1; ++v) {
+                const unsigned k = keys[v];
+                if (k == kHitKey) continue;
+                if (k < thr) ++nv;
+                else if (k == thr && er++ < need) ++nv;
+            }
+        }
+        int nv_total;
+        int vpos = block_exclusive_scan(nv, s_tmp, &nv_total);
+        {
+            int er = eq_before;
+            for (int v = v0; v < v1; ++v) {
+                const unsigned k = keys[v];
+                if (k == kHitKey) continue;
+                bool take = false;
+                if (k < thr) take = true;
+                else if (k == thr && er++ < need) take = true;
+                if (take) vict[vpos++] = v;
+            }
+        }
+        // ---- admitted misses ---------------------------------------------------
+        if (U > cap) {
+            const int* last = a.ws.miss_last + wbase;
+            if (tid < 8) s_misc[tid] = 0;
+            __syncthreads();
+            for (int j = tid; j < U; j += BD) atomicAdd(&s_misc[last[j]], 1);
+            __syncthreads();
+            // threshold step: walk from the latest step down
+            int s_thr = 0, need_s = m, acc = 0;
+            for (int s = a.S - 1; s >= 0; --s) {
+                if (acc + s_misc[s] >= m) {
+                    s_thr = s;
+                    need_s = m - acc;
+                    break;
+                }
+                acc += s_misc[s];
+            }
+            const int segj = (U + BD - 1) / BD;
+            const int j0 = tid * segj, j1 = min(U, j0 + segj);
+            int eqs = 0;
+            for (int j = j0; j < j1; ++j) eqs += (last[j] == s_thr);
+            int eqs_total;
+            int er = block_exclusive_scan(eqs, s_tmp, &eqs_total);
+            int na = 0;
+            {
+                int r = er;
+                for (int j = j0; j < j1; ++j) {
+                    const int l = last[j];
+                    if (l > s_thr || (l == s_thr && r++ < need_s)) ++na;
+                }
+            }
+            int na_total;
+            int apos = block_exclusive_scan(na, s_tmp, &na_total);
+            for (int j = j0; j < j1; ++j) {
+                const int l = last[j];
+                if (l > s_thr || (l == s_thr && er++ < need_s)) adm[apos++] = j;
+            }
+        }
+        __syncthreads();
+        // ---- evict: the victims' old tokens leave the hash --------------------
+        for (int i = tid; i < m; i += BD) {
+            const int v = vict[i];
+            const int old = tok[v];
+            if (old >= 0) {
+                bank_delete(bank, d.hash_shift, hmask, old, a.ws.status);
+                ++evicted;
+            }
+        }
+        evicted = block_sum(evicted, s_tmp);  // barrier: all deletions done
+        // ---- rotate and admit --------------------------------------------------
+        int fresh = 0;
+        const int32_t* mtok = a.ws.miss_tok + wbase;
+        for (int i = tid; i < m; i += BD) {
+            const int v = vict[i];
+            const int j = (U > cap) ? adm[i] : i;
+            const int p = phys[v];
+            phys[v] = phys[H + j];
+            phys[H + j] = p;
+            const int t = mtok[j];
+            tok[v] = t;
+            ep[v] = E;
+            fresh += bank_insert(bank, d.hash_shift, hmask, t, v, a.ws.status);
+        }
+        fresh = block_sum(fresh, s_tmp);
+        if (tid == 0) {
+            s_misc[0] = ctrl[CTRL_USED] + fresh;
+            s_misc[1] = ctrl[CTRL_RESIDENT] + m - evicted;
+        }
+        __syncthreads();
+        // ---- rebuild the bank once deleted entries pile up ---------------------
+        if (s_misc[0] > (d.hash_size / 4) * 3) {
+            for (int p = tid; p < d.hash_size; p += BD) bank[p] = kEmpty;
+            __syncthreads();
+            for (int v = tid; v < H; v += BD) {
+                const int t = tok[v];
+                if (t >= 0) bank_insert(bank, d.hash_shift, hmask, t, v, a.ws.status);
+            }
+            if (tid == 0) {
+                s_misc[0] = s_misc[1];
+                ctrl[CTRL_REBUILDS] += 1;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            ctrl[CTRL_USED] = s_misc[0];
+            ctrl[CTRL_RESIDENT] = s_misc[1];
+        }
+    }
+    if (tid == 0) {
+        ctrl[CTRL_EPOCH] = E + 1;
+        ctrl[CTRL_LOCK] = 0;
+        if (a.stats) {
+            int32_t* st = a.stats + (long long)b * HS_NUM_STATS;
+            st[HS_STAT_HIT_SLOTS] = nhit;
+            st[HS_STAT_ADMITTED] = m;
+            st[HS_STAT_EVICTED] = evicted;
+            st[HS_STAT_OVERFLOW] = U - m;
+        }
+    }
+}
+
+__device__ void copy_rows(const SwapArgs& a, int cta, int ncta, int* pre) {
+    __shared__ int s_tmp[33];
+    const Dims& d = a.d;
+    const int tid = threadIdx.x, BD = blockDim.x;
+    const int B = a.B;
+    // Exclusive prefix of the unique-miss counts over the batch rows.
+    const int per = (B + BD - 1) / BD;
+    const int b0 = tid * per, b1 = min(B, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += a.ws.cnt[(long long)b * kCntWords + CNT_U];
+    int total;
+    int run = block_exclusive_scan(sum, s_tmp, &total);
+    for (int b = b0; b < b1; ++b) {
+        pre[b] = run;
+        run += a.ws.cnt[(long long)b * kCntWords + CNT_U];
+    }
+    if (tid == 0) pre[B] = total;
+    __syncthreads();
+    if (total == 0) return;
+
+    const int nv = d.W >> 4;  // 16-byte pieces per row
+    const long long chunks = (long long)total * nv;
+    const long long span = (chunks + ncta - 1) / ncta;
+    const long long c0 = (long long)cta * span;
+    const long long c1 = min(chunks, c0 + span);
+    const uint8_t* pool = a.lv.host_pool;
+    uint8_t* kv = a.lv.device_kv;
+    for (long long g = c0; g < c1; g += (long long)BD * kCopyUnroll) {
+        uint4 v[kCopyUnroll];
+        int drow[kCopyUnroll];  // destination row of each piece, -1 if none
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const long long c = g + (long long)u * BD + tid;
+            drow[u] = -1;
+            if (c < c1) {
+                const int row = (int)(c / nv);
+                const int piece = (int)(c - (long long)row * nv);
+                int lo = 0, hi = B;  // last b with pre[b] <= row
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (pre[mid] <= row) lo = mid;
+                    else hi = mid;
+                }
+                const long long wi = (long long)lo * d.C + (row - pre[lo]);
+                const int q = a.ws.cnt[(long long)lo * kCntWords + CNT_Q];
+                const long long src =
+                    ((long long)q * d.L + a.ws.miss_tok[wi]) * d.W + ((long long)piece << 4);
+                drow[u] = a.ws.miss_dst[wi];
+                v[u] = ld_stream_v4(pool + src);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            if (drow[u] < 0) continue;
+            const long long c = g + (long long)u * BD + tid;
+            const long long piece = c - (c / nv) * nv;
+            st_v4(kv + (long long)drow[u] * d.W + (piece << 4), v[u]);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kBlock, 2) commit_copy_kernel(const SwapArgs a, int copy_ctas) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    pdl_wait();  // the gather grid's results are visible after this
+    if ((int)blockIdx.x < a.B)
+        commit_request(a, blockIdx.x, reinterpret_cast<unsigned*>(smem));
+    else
+        copy_rows(a, blockIdx.x - a.B, copy_ctas, reinterpret_cast<int*>(smem));
+}
+
+}  // namespace
+
+size_t commit_smem_bytes(const Dims& d) {
+    const size_t keys = (size_t)d.H * 4;
+    const size_t pre = (size_t)(d.B_max + 1) * 4;
+    return keys > pre ? keys : pre;
+}
+
+cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s) {
+    static int cached = 48 * 1024;
+    const size_t smem = commit_smem_bytes(a.d);
+    cudaError_t e = ensure_smem(commit_copy_kernel, smem, &cached);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.B + copy_ctas);
+    cfg.blockDim = dim3(kBlock);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, commit_copy_kernel, a, copy_ctas);
+}
+
+}  // namespace hs

@@ -1,0 +1,191 @@
+// Internal layout and launch interface of the GB300 swap-in library.
+//
+// Device memory is caller-owned and carved here into:
+//   state (persistent, per layer l and request q):
+//     bank  int64 [layers][R][hash_size]  token -> slot hash, (t << 32) | slot;
+//                                         -1 never used, -2 deleted
+//     ep    int32 [layers][R][H]          epoch of the slot's last reference
+//     tok   int32 [layers][R][H]          token held by the slot (-1 empty)
+//     phys  int32 [layers][R][H + C]      physical row of each position
+//     ctrl  int32 [layers][R][8]          control words (see Ctrl)
+//   workspace (one call at a time, shared by all layers):
+//     miss_tok / miss_last / miss_dst / vict / adm  int32 [B_max][C]
+//     cnt   int32 [B_max][16]             per-request call counters
+//     status uint32                       sticky device status flags
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hisparse_swap.h"
+
+namespace hs {
+
+constexpr long long kEmpty = -1;    // hash entry never used
+constexpr long long kDeleted = -2;  // hash entry deleted (probe continues)
+
+constexpr int kCtrlWords = 8;
+enum Ctrl : int {
+    CTRL_EPOCH = 0,     // epoch of the next call
+    CTRL_RESIDENT = 1,  // tokens resident in the hot slots
+    CTRL_USED = 2,      // hash entries not empty (live + deleted)
+    CTRL_LOCK = 3,      // held from gather to commit of one call
+    CTRL_REBUILDS = 4,  // hash rebuilds so far (diagnostic)
+};
+
+constexpr int kCntWords = 16;
+enum Cnt : int {
+    CNT_U = 0,        // unique misses
+    CNT_HITS = 1,     // hit entries
+    CNT_MISSES = 2,   // miss entries (unique + duplicates)
+    CNT_INVALID = 3,  // invalid entries
+    CNT_SKIP = 4,     // 1 if this batch row was rejected on the device
+    CNT_Q = 5,        // request slot of this batch row
+};
+
+struct Dims {
+    int32_t R, L, W, H, K, S_max, C, layers, B_max;
+    int32_t hash_size;   // entries per request bank, power of two (>= 32)
+    int32_t hash_shift;  // 32 - log2(hash_size)
+};
+
+struct LayerView {
+    long long* bank;           // [R][hash_size]
+    int32_t* ep;               // [R][H]
+    int32_t* tok;              // [R][H]
+    int32_t* phys;             // [R][H + C]
+    int32_t* ctrl;             // [R][kCtrlWords]
+    const uint8_t* host_pool;  // device mapping of the pinned pool [R][L][W]
+    uint8_t* device_kv;        // [R][H + C][W]
+};
+
+struct Workspace {
+    int32_t* miss_tok;   // [B_max][C] token of unique miss j
+    int32_t* miss_last;  // [B_max][C] last step in which miss j occurs
+    int32_t* miss_dst;   // [B_max][C] device row miss j was written to
+    int32_t* vict;       // [B_max][C] victims in ascending slot order
+    int32_t* adm;        // [B_max][C] admitted ordinals in ascending order
+    int32_t* cnt;        // [B_max][kCntWords]
+    uint32_t* status;    // sticky HS_STATUS_* flags
+};
+
+struct SwapArgs {
+    Dims d;
+    LayerView lv;
+    Workspace ws;
+    const int32_t* rpi;       // [B]
+    const int32_t* seq_lens;  // [B]
+    const int32_t* topk;      // [B][S][K]
+    int32_t B, S;
+    int32_t* locs;      // [B][S][K]
+    int32_t* stats;     // [B][HS_NUM_STATS] or null
+    long long* plan_src;  // [B][C] or null
+    long long* plan_dst;  // [B][C] or null
+    int32_t* plan_count;  // [B] or null
+    int32_t dedup_size;   // gather's shared-memory dedup table entries (power of two)
+    int32_t dedup_shift;  // 32 - log2(dedup_size)
+};
+
+// Byte offsets of the state and workspace regions (256-byte aligned).
+struct StateLayout {
+    size_t bank, ep, tok, phys, ctrl, total;
+};
+struct WorkspaceLayout {
+    size_t miss_tok, miss_last, miss_dst, vict, adm, cnt, status, total;
+};
+
+StateLayout state_layout(const Dims& d);
+WorkspaceLayout workspace_layout(const Dims& d);
+LayerView layer_view(const Dims& d, uint8_t* state, int layer, const uint8_t* host_pool,
+                     uint8_t* device_kv);
+Workspace workspace_view(const Dims& d, uint8_t* ws);
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes`
+// (remembered in `*cached`, so repeated calls cost nothing).
+template <typename F>
+cudaError_t ensure_smem(F* kernel, size_t bytes, int* cached) {
+    if ((int)bytes <= *cached) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) *cached = (int)bytes;
+    return e;
+}
+
+// Launchers (each returns the launch's error code).
+size_t gather_smem_bytes(int entries, int* dedup_size);
+cudaError_t launch_gather(const SwapArgs& a, cudaStream_t s);
+size_t commit_smem_bytes(const Dims& d);
+cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s);
+cudaError_t launch_reset(const Dims& d, uint8_t* state, const int32_t* rpi, int32_t n,
+                         cudaStream_t s);
+cudaError_t launch_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t B,
+                              int32_t S, int32_t K, int32_t L_max, int32_t page_size,
+                              int32_t* pages, int32_t* num_pages, int32_t* token_page,
+                              cudaStream_t s);
+
+// ---- device helpers shared by the kernels -----------------------------------
+#ifdef __CUDACC__
+
+// Multiplicative (Fibonacci) hash of a token into a table of 2^(32 - shift)
+// entries: the top bits of t * 2^32 / golden ratio.
+__device__ __forceinline__ uint32_t hash_token(int32_t t, int shift) {
+    return ((uint32_t)t * 0x9E3779B9u) >> shift;
+}
+
+__device__ __forceinline__ long long make_entry(int32_t t, int32_t slot) {
+    return ((long long)t << 32) | (uint32_t)slot;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Programmatic dependent launch controls (sm_90 and later).
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Inclusive warp scan.
+__device__ __forceinline__ int warp_inclusive_scan(int x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// Exclusive block scan of one int per thread; returns the prefix and the
+// block total.  `tmp` needs 33 ints of shared memory.  All threads call it.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* tmp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    int inc = warp_inclusive_scan(x);
+    if (lane == 31) tmp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? tmp[lane] : 0;
+        int wi = warp_inclusive_scan(w);
+        tmp[lane] = wi - w;
+        if (lane == 31) tmp[32] = wi;
+    }
+    __syncthreads();
+    int r = tmp[warp] + inc - x;
+    *total = tmp[32];
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ int block_sum(int x, int* tmp) {
+    int total;
+    block_exclusive_scan(x, tmp, &total);
+    return total;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace hs

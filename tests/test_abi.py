@@ -1,0 +1,126 @@
+"""The C ABI library on the CPU: it builds, loads, exports every symbol that
+include/hisparse_swap.h declares, and validates arguments before touching CUDA."""
+import ctypes
+
+import pytest
+
+import sparse_attention_kv_swap_gb300 as pkg
+from sparse_attention_kv_swap_gb300 import binding as B
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_kv_swap_gb300 import build
+    build.build()
+    return B.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = B.header_symbols()
+    assert len(names) >= 14
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_header_constants_match_binding():
+    import re
+    text = open(B.HEADER).read()
+    consts = dict(re.findall(r"#define (HS_[A-Z_0-9]+) \(?(-?(?:0x)?[0-9a-fA-F]+)u?\)?", text))
+    for name in ("HS_OK", "HS_ERR_INVALID_ARG", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
+                 "HS_ERR_DEVICE_STATUS", "HS_ERR_TIMEOUT", "HS_STATUS_BAD_REQUEST",
+                 "HS_STATUS_DUPLICATE_REQUEST", "HS_STATUS_SEQ_LEN_CLAMPED",
+                 "HS_STATUS_PROBE_LIMIT", "HS_STATUS_TABLE_FULL", "HS_NUM_STATS"):
+        assert int(consts[name], 0) == getattr(B, name), name
+
+
+def test_version_and_strings(lib):
+    assert pkg.hs_version() == 100
+    assert pkg.hs_status_string(0) == "ok"
+    assert "invalid" in pkg.hs_status_string(-1)
+    assert pkg.hs_status_string(-99) == "unknown status"
+
+
+def _cfg(**kw):
+    base = dict(num_requests=64, max_seq_len=32768, item_size_bytes=656, hot_buffer_size=8192,
+                top_k=2048, max_steps=4, num_layers=1, max_batch=64)
+    base.update(kw)
+    return B.HsConfig(**base)
+
+
+def test_config_check(lib):
+    assert pkg.hs_config_check(_cfg()) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(item_size_bytes=650)) == B.HS_ERR_INVALID_ARG
+    assert pkg.hs_config_check(_cfg(hot_buffer_size=32769)) == B.HS_ERR_UNSUPPORTED
+    assert pkg.hs_config_check(_cfg(hot_buffer_size=32768)) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(max_steps=5)) == B.HS_ERR_UNSUPPORTED
+    assert pkg.hs_config_check(_cfg(top_k=4096)) == B.HS_ERR_UNSUPPORTED
+    assert pkg.hs_config_check(_cfg(max_steps=2, top_k=4096)) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(max_batch=65)) == B.HS_ERR_INVALID_ARG
+    assert pkg.hs_config_check(_cfg(num_layers=0)) == B.HS_ERR_INVALID_ARG
+    assert lib.hs_config_check(None) == B.HS_ERR_INVALID_ARG
+
+
+def test_sizes(lib):
+    c = _cfg()
+    H, C, R = 8192, 8192, 64
+    assert pkg.hs_hash_size(c) == 16384
+    assert pkg.hs_device_kv_bytes(c) == R * (H + C) * 656
+    assert pkg.hs_host_pool_bytes(c) == R * 32768 * 656
+    st = pkg.hs_state_bytes(c)
+    assert st >= R * (16384 * 8 + H * 4 * 2 + (H + C) * 4 + 32)
+    assert st % 256 == 0
+    assert pkg.hs_workspace_bytes(c) >= 5 * 64 * C * 4
+    assert pkg.hs_state_bytes(_cfg(max_steps=9)) == 0
+    assert pkg.hs_hash_size(_cfg(hot_buffer_size=1)) == 32
+
+
+def test_create_rejects_bad_arguments_without_cuda(lib):
+    c = _cfg(num_requests=2, max_seq_len=16, hot_buffer_size=4, top_k=2, max_steps=1,
+             max_batch=2)
+    out = ctypes.c_void_p()
+    arr = (ctypes.c_void_p * 1)(0x1000)
+    rc = lib.hs_create_state(ctypes.byref(c), arr, arr, None, 0, None, 0, None, ctypes.byref(out))
+    assert rc == B.HS_ERR_INVALID_ARG and not out.value
+    big = 1 << 20
+    rc = lib.hs_create_state(ctypes.byref(c), arr, arr, ctypes.c_void_p(0x100000), 8,
+                             ctypes.c_void_p(0x200000), big, None, ctypes.byref(out))
+    assert rc == B.HS_ERR_INVALID_ARG  # state smaller than hs_state_bytes
+    rc = lib.hs_create_state(ctypes.byref(c), arr, arr, ctypes.c_void_p(0x100010), big,
+                             ctypes.c_void_p(0x200000), big, None, ctypes.byref(out))
+    assert rc == B.HS_ERR_INVALID_ARG  # state not 256-byte aligned
+    bad = (ctypes.c_void_p * 1)(0x1001)
+    rc = lib.hs_create_state(ctypes.byref(c), bad, arr, ctypes.c_void_p(0x100000), big,
+                             ctypes.c_void_p(0x200000), big, None, ctypes.byref(out))
+    assert rc == B.HS_ERR_INVALID_ARG  # host pool not 16-byte aligned
+    assert lib.hs_create_state(ctypes.byref(c), arr, arr, None, 0, None, 0, None, None) == \
+        B.HS_ERR_INVALID_ARG
+
+
+def test_calls_reject_null_handle(lib):
+    assert lib.hs_swap_in(None, None, None, None, 1, 1, 0, None, None, None, None, None,
+                          None) == B.HS_ERR_INVALID_ARG
+    assert lib.hs_reset_requests(None, None, 1, None) == B.HS_ERR_INVALID_ARG
+    flags = ctypes.c_uint32()
+    assert lib.hs_get_status(None, ctypes.byref(flags), None) == B.HS_ERR_INVALID_ARG
+    assert lib.hs_export_request_state(None, 0, 0, None, None, None, None, None, None) == \
+        B.HS_ERR_INVALID_ARG
+    lib.hs_destroy_state(None)
+
+
+def test_page_table_rejects_bad_arguments(lib):
+    assert lib.hs_page_table(None, None, 1, 0, 4, 100, 16, None, None, None, None) == \
+        B.HS_ERR_INVALID_ARG
+    assert lib.hs_page_table(None, None, 1, 1, 4, 100, 0, None, None, None, None) == \
+        B.HS_ERR_INVALID_ARG
+    assert lib.hs_page_table(None, None, 1, 4, 4096, 100, 16, None, None, None, None) == \
+        B.HS_ERR_UNSUPPORTED
+    assert lib.hs_page_table(None, None, 1, 1, 4, 1 << 30, 1, None, None, None, None) == \
+        B.HS_ERR_UNSUPPORTED
+    assert lib.hs_page_table(None, None, 0, 1, 4, 100, 16, None, None, None, None) == B.HS_OK
+    assert lib.hs_page_table(None, None, 2, 1, 4, 100, 16, None, None, None, None) == \
+        B.HS_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        B.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,150 @@
+"""Page table, device status flags, argument errors and graph capture on the GPU."""
+import numpy as np
+import pytest
+import torch
+
+import hs_workloads as W
+import sparse_attention_kv_swap_gb300 as pkg
+from sparse_attention_kv_swap_gb300 import binding as B
+from gpu_harness import ParityRun
+
+pytestmark = pytest.mark.gpu
+
+
+def _page_table_gpu(topk, sl, L_max, page):
+    B_, S, K = topk.shape
+    pages = torch.empty((B_, S * K), dtype=torch.int32, device="cuda")
+    num = torch.empty(B_, dtype=torch.int32, device="cuda")
+    tp = torch.empty((B_, S, K), dtype=torch.int32, device="cuda")
+    B.hs_page_table(torch.from_numpy(topk).cuda(), torch.from_numpy(sl).cuda(), L_max, page,
+                    pages, num, tp)
+    torch.cuda.synchronize()
+    return pages.cpu().numpy(), num.cpu().numpy(), tp.cpu().numpy()
+
+
+@pytest.mark.parametrize("page", [1, 7, 64, 256])
+def test_page_table_random(page):
+    from oracle import page_table
+    rng = np.random.default_rng(page)
+    for trial in range(5):
+        Bn, S, K = 3, int(rng.integers(1, 5)), int(rng.integers(1, 700))
+        L = int(rng.integers(1, 20000))
+        topk = rng.integers(-3, L + 40, size=(Bn, S, K)).astype(np.int32)
+        sl = rng.integers(1, L + 20, size=Bn).astype(np.int32)
+        got = _page_table_gpu(topk, sl, L, page)
+        ref = page_table(topk, sl, page, max_seq_len=L)
+        for g, r in zip(got, ref):
+            assert (g == r).all()
+
+
+def test_page_table_long_context_workload():
+    from oracle import page_table
+    w = W.WORKLOADS["C5"]
+    stream = W.TopkStream(w)
+    sl = W.seq_lens(w)
+    for c in range(4):
+        topk = stream.next_call()
+        got = _page_table_gpu(topk, sl, w.seq_len, w.page_size)
+        ref = page_table(topk, sl, w.page_size, max_seq_len=w.seq_len)
+        for g, r in zip(got, ref):
+            assert (g == r).all()
+        assert got[1].max() < 200  # clustered selections touch few pages
+
+
+def test_status_flags():
+    run = ParityRun(3, 100, 32, 8, 4, 1)
+    cache = run.cache
+    topk = torch.zeros((2, 1, 4), dtype=torch.int32, device="cuda")
+    sl = torch.full((2,), 100, dtype=torch.int32, device="cuda")
+    cache.swap_in(torch.tensor([1, 1], dtype=torch.int32, device="cuda"), sl, topk)
+    rc, flags = cache.status()
+    assert rc == B.HS_ERR_DEVICE_STATUS and flags & B.HS_STATUS_DUPLICATE_REQUEST
+    assert cache.status() == (0, 0)  # reading clears the flags
+    cache.swap_in(torch.tensor([0, 7], dtype=torch.int32, device="cuda"), sl, topk)
+    rc, flags = cache.status()
+    assert flags & B.HS_STATUS_BAD_REQUEST
+    out = cache.swap_in(torch.tensor([0, 2], dtype=torch.int32, device="cuda"),
+                        torch.tensor([100, 500], dtype=torch.int32, device="cuda"), topk)
+    rc, flags = cache.status()
+    assert flags == B.HS_STATUS_SEQ_LEN_CLAMPED
+    # locks were released: a normal call still works and raises nothing
+    cache.swap_in(torch.tensor([1, 2], dtype=torch.int32, device="cuda"), sl, topk)
+    assert cache.status() == (0, 0)
+
+
+def test_argument_errors():
+    run = ParityRun(2, 100, 32, 8, 4, 2, max_batch=2)
+    c = run.cache
+    i32 = dict(dtype=torch.int32, device="cuda")
+    rpi = torch.tensor([0, 1], **i32)
+    sl = torch.tensor([100, 100], **i32)
+    with pytest.raises(pkg.HsError) as e:
+        c.swap_in(rpi, sl, torch.zeros((2, 3, 4), **i32))  # 3 steps > max_steps
+    assert e.value.code == B.HS_ERR_INVALID_ARG
+    with pytest.raises(pkg.HsError):
+        c.swap_in(rpi, sl, torch.zeros((2, 1, 4), **i32), layer_id=1)
+    with pytest.raises(pkg.HsError):
+        c.swap_in(torch.tensor([0, 1, 1], **i32), torch.tensor([1, 1, 1], **i32),
+                  torch.zeros((3, 1, 4), **i32))  # batch > max_batch
+    locs = torch.empty((2, 1, 4), **i32)
+    src = torch.empty((2, 8), dtype=torch.int64, device="cuda")
+    with pytest.raises(pkg.HsError):  # a partial miss plan
+        B.hs_swap_in(c.handle, rpi, sl, torch.zeros((2, 1, 4), **i32), 0, locs, None, src)
+
+
+def test_pageable_pool_rejected_or_served_exactly():
+    """Pageable host memory is refused unless the device reads host page
+    tables directly; where it is accepted, rows still arrive bit-exact."""
+    cfg = pkg.make_config(1, 64, 32, 4, 2, 1)
+    pool = torch.empty((1, 64, 32), dtype=torch.uint8)  # pageable
+    W.fill_host_pool(pool.numpy(), 0)
+    kv = torch.zeros((1 * 6, 32), dtype=torch.uint8, device="cuda")
+    st = torch.empty(pkg.hs_state_bytes(cfg), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(pkg.hs_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    try:
+        h = pkg.hs_create_state(cfg, [pool], [kv], st, ws)
+    except pkg.HsError as e:
+        assert e.code == B.HS_ERR_INVALID_ARG
+        return
+    i32 = dict(dtype=torch.int32, device="cuda")
+    locs = torch.empty((1, 1, 2), **i32)
+    B.hs_swap_in(h, torch.tensor([0], **i32), torch.tensor([64], **i32),
+                 torch.tensor([[[7, 63]]], **i32), 0, locs)
+    torch.cuda.synchronize()
+    rows = kv[locs.view(-1).long()].cpu().numpy()
+    assert (rows == W.host_rows(0, [0, 0], [7, 63], 32)).all()
+    h.close()
+
+
+def test_cuda_graph_replay_matches_direct():
+    """A captured call replays to the same outputs and state as direct calls."""
+    rng = np.random.default_rng(21)
+    a = ParityRun(4, 4000, W.ROW_BYTES, 256, 256, 2)
+    b = ParityRun(4, 4000, W.ROW_BYTES, 256, 256, 2, pools=a.pools)
+    rpi = torch.tensor([3, 1, 0, 2], dtype=torch.int32, device="cuda")
+    sl = torch.full((4,), 4000, dtype=torch.int32, device="cuda")
+    topk_buf = torch.empty((4, 2, 256), dtype=torch.int32, device="cuda")
+    out = {"device_locs": torch.empty((4, 2, 256), dtype=torch.int32, device="cuda"),
+           "stats": torch.empty((4, 8), dtype=torch.int32, device="cuda")}
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b.cache.swap_in(rpi, sl, topk_buf.zero_(), stats=True, out=out, stream=s)  # warm-up
+        b.cache.reset_requests(torch.arange(4, dtype=torch.int32, device="cuda"), stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.cache.swap_in(rpi, sl, topk_buf, stats=True, out=out, stream=s)
+    b.cache.reset_requests(torch.arange(4, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    for c in range(5):
+        topk = rng.integers(0, 4000, size=(4, 2, 256)).astype(np.int32)
+        ga = a.call(topk, rpi.cpu().numpy(), sl.cpu().numpy())
+        topk_buf.copy_(torch.from_numpy(topk))
+        g.replay()
+        torch.cuda.synchronize()
+        assert (out["device_locs"].cpu().numpy() == ga["device_locs"]).all()
+        assert (out["stats"].cpu().numpy() == ga["stats"]).all()
+    for q in range(4):
+        sa, sb = a.gpu_state(0, q), b.gpu_state(0, q)
+        for k in ("tok", "ep", "phys"):
+            assert (sa[k] == sb[k]).all()

@@ -1,0 +1,135 @@
+"""CUDA path against the CPU oracle, bit for bit (needs a GB300).
+
+Small cases span several gather tiles (1024 entries per tile row), ragged
+top-k widths, every step count, overflow and multiple layers; the workload
+cases run the five configurations' index streams, scaled where marked and at
+full size where the oracle still finishes in seconds.
+"""
+import numpy as np
+import pytest
+
+import hs_workloads as W
+from gpu_harness import ParityRun
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand_calls(rng, R, L, K, S_max, B, calls, reuse=0.5, invalid=0.05):
+    prev = None
+    for c in range(calls):
+        S = int(rng.integers(1, S_max + 1))
+        topk = rng.integers(0, L, size=(B, S, K)).astype(np.int32)
+        if prev is not None:
+            n = int(reuse * K)
+            topk[:, 0, :n] = prev[:, -1, -n:]
+        for s in range(1, S):
+            n = int(reuse * K)
+            topk[:, s, :n] = topk[:, s - 1, K - n:]
+        mask = rng.random(topk.shape) < invalid
+        topk[mask] = rng.choice([-1, L, L + 7, -5], size=int(mask.sum()))
+        rpi = rng.permutation(R)[:B].astype(np.int32)
+        sl = rng.integers(L // 2, L + 1, size=B).astype(np.int32)
+        prev = topk
+        yield topk, rpi, sl
+
+
+SMALL = [
+    # R, L, H, K, S_max, B, calls
+    (1, 256, 16, 8, 1, 1, 12),
+    (3, 500, 40, 37, 4, 3, 10),      # ragged K, all step counts
+    (4, 2000, 300, 300, 4, 4, 8),    # several 1024-entry tiles per request
+    (2, 9000, 1000, 2048, 4, 2, 6),  # 8192 entries per request (largest tile count)
+    (5, 3000, 64, 600, 3, 5, 6),     # heavy overflow
+    (2, 100, 1, 5, 2, 2, 10),        # a single hot slot
+    (6, 70000, 512, 513, 2, 4, 5),   # long rows, ragged tile tail
+]
+
+
+@pytest.mark.parametrize("R,L,H,K,S_max,B,calls", SMALL)
+def test_small_configs(R, L, H, K, S_max, B, calls):
+    rng = np.random.default_rng(R * 1000 + K)
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max)
+    for topk, rpi, sl in _rand_calls(rng, R, L, K, S_max, B, calls):
+        run.call(topk, rpi, sl, properties=True)
+
+
+def test_two_layers_interleaved():
+    rng = np.random.default_rng(5)
+    run = ParityRun(3, 800, W.ROW_BYTES, 64, 48, 2, layers=2)
+    gens = [_rand_calls(rng, 3, 800, 48, 2, 3, 6), _rand_calls(rng, 3, 800, 48, 2, 3, 6)]
+    for c in range(6):
+        for layer in (1, 0):
+            topk, rpi, sl = next(gens[layer])
+            run.call(topk, rpi, sl, layer=layer)
+
+
+def test_miss_plan_matches():
+    rng = np.random.default_rng(9)
+    run = ParityRun(4, 1000, W.ROW_BYTES, 100, 64, 4)
+    for topk, rpi, sl in _rand_calls(rng, 4, 1000, 64, 4, 4, 5):
+        run.call(topk, rpi, sl, plan=True)
+
+
+def test_reset_requests_matches():
+    import torch
+    rng = np.random.default_rng(11)
+    run = ParityRun(4, 600, W.ROW_BYTES, 50, 32, 2, layers=2)
+    calls = list(_rand_calls(rng, 4, 600, 32, 2, 4, 6))
+    for i, (topk, rpi, sl) in enumerate(calls):
+        run.call(topk, rpi, sl, layer=i % 2)
+        if i == 3:
+            victims = np.array([1, 3], np.int32)
+            run.cache.reset_requests(torch.from_numpy(victims).cuda())
+            run.oracle.reset_requests(victims)
+            for layer in range(2):
+                for q in victims.tolist():
+                    g = run.gpu_state(layer, q)
+                    assert (g["tok"] == -1).all() and g["epoch"] == 0
+                    assert (g["phys"] == np.arange(50 + 64)).all()
+
+
+def test_batch_zero_and_all_invalid():
+    import torch
+    run = ParityRun(2, 100, W.ROW_BYTES, 8, 4, 1)
+    empty = torch.empty((0, 1, 4), dtype=torch.int32, device="cuda")
+    e32 = torch.empty(0, dtype=torch.int32, device="cuda")
+    out = run.cache.swap_in(e32, e32, empty)
+    assert out["device_locs"].numel() == 0
+    topk = np.array([[[-1, 100, 200, -7]], [[5, 5, -1, 99]]], np.int32)
+    g = run.call(topk, np.array([0, 1], np.int32), np.array([100, 50], np.int32))
+    assert (g["device_locs"][0] == -1).all()
+
+
+def test_hot_buffer_upper_bound():
+    # 32768 hot slots (the multi-step report's stated bound), 8192 entries per call
+    rng = np.random.default_rng(13)
+    run = ParityRun(1, 70000, 64, 32768, 2048, 4)
+    for c in range(4):
+        topk = np.stack([rng.permutation(70000)[:2048] for _ in range(4)])[None]
+        run.call(topk.astype(np.int32), np.array([0], np.int32), np.array([70000], np.int32))
+
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C5"])
+def test_workload_scaled(name):
+    w = W.WORKLOADS[name]
+    if name != "C1":
+        w = W.scaled(w, batch=4, seq_len=min(w.seq_len, 16384))
+    stream = W.TopkStream(w)
+    rpi = W.req_pool_indices(w)
+    sl = W.seq_lens(w)
+    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps)
+    for c in range(w.calls if name == "C1" else 10):
+        run.call(stream.next_call(), rpi, sl, properties=(name == "C4"))
+
+
+@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5"])
+def test_workload_full_size(name):
+    """Full-size configuration, every output compared (8 calls of the stream)."""
+    w = W.WORKLOADS[name]
+    stream = W.TopkStream(w)
+    rpi = W.req_pool_indices(w)
+    sl = W.seq_lens(w)
+    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps)
+    for c in range(8):
+        run.call(stream.next_call(), rpi, sl, compare_rows=(c % 4 == 3),
+                 properties=(name == "C4" and c == 7))
