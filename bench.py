@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--copy-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--compare-sequential", action="store_true",
+                    help="multi-step vs sequential per-step swap under CUDA graphs")
     return ap.parse_args()
 
 
@@ -216,6 +218,93 @@ def run_reference(args, w):
     return 0
 
 
+def run_compare_sequential(args, w):
+    """Multi-step swap (one S-step call) against sequential per-step swap (S
+    single-step calls) on the same index stream, each captured as a CUDA
+    graph, as in the multi-step swap report's benchmark (section 实现拆解
+    item 4; its 48.2% figure is for batch 64, 4 steps on an H20)."""
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    from sparse_attention_kv_swap_gb300.cache import SwapInCache
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    K, Wm = args.steps, args.warmup
+    calls = W.TopkStream(w).calls(PREROLL_CALLS + Wm + K)
+    cfg = pkg.make_config(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, 1)
+    pool = torch.empty((w.batch, w.seq_len, w.row_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_host_pool(pool.numpy(), 0)
+    multi = SwapInCache(cfg, host_pools=[pool], device=dev)
+    seq = SwapInCache(cfg, host_pools=[pool], device=dev)
+    rpi = torch.from_numpy(W.req_pool_indices(w)).to(dev)
+    sl = torch.from_numpy(W.seq_lens(w)).to(dev)
+    Bn, S, Kk = w.batch, w.steps, w.top_k
+    buf_m = torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)
+    buf_s = [torch.empty((Bn, 1, Kk), dtype=torch.int32, device=dev) for _ in range(S)]
+    out_m = {"device_locs": torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)}
+    out_s = [{"device_locs": torch.empty((Bn, 1, Kk), dtype=torch.int32, device=dev)}
+             for _ in range(S)]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+
+    def load(c):
+        t = torch.from_numpy(c).to(dev)
+        buf_m.copy_(t)
+        for s in range(S):
+            buf_s[s].copy_(t[:, s:s + 1])
+
+    def run_multi():
+        multi.swap_in(rpi, sl, buf_m, 0, out=out_m, stream=stream)
+
+    def run_seq():
+        for s in range(S):
+            seq.swap_in(rpi, sl, buf_s[s], 0, out=out_s[s], stream=stream)
+
+    load(calls[0])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):  # first calls set kernel attributes outside capture
+        run_multi()
+        run_seq()
+    torch.cuda.synchronize()
+    multi.reset_requests(torch.arange(Bn, dtype=torch.int32, device=dev))
+    seq.reset_requests(torch.arange(Bn, dtype=torch.int32, device=dev))
+    g_multi, g_seq = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_multi, stream=stream):
+        run_multi()
+    with torch.cuda.graph(g_seq, stream=stream):
+        run_seq()
+    torch.cuda.synchronize()
+    t_m, t_s = [], []
+    for i, c in enumerate(calls):
+        load(c)
+        torch.cuda.synchronize()
+        timed = i >= PREROLL_CALLS + Wm
+        for g, acc in ((g_multi, t_m), (g_seq, t_s)):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            if timed:
+                acc.append(a.elapsed_time(b))
+    for cache in (multi, seq):
+        rc, flags = cache.status()
+        if flags:
+            raise RuntimeError("device status flags %#x" % flags)
+    ms_m, ms_s = statistics.mean(t_m), statistics.mean(t_s)
+    line = {"metric": "multi-step vs sequential per-step swap latency reduction",
+            "value": 1.0 - ms_m / ms_s, "unit": "fraction", "higher_is_better": True,
+            "multi_step_ms": ms_m, "sequential_ms": ms_s,
+            "multi_step_tokens_per_s": w.entries / (ms_m * 1e-3),
+            "sequential_tokens_per_s": w.entries / (ms_s * 1e-3),
+            "steps": K, "warmup": Wm, "cuda_graph": True, "data": "synthetic",
+            "config": config_dict(w, 1),
+            "context": "pages: 48.2% at batch 64, 4 steps, H20 (Hopper)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def config_dict(w, world):
     return {"workload": "%s (%s)" % (w.name, "C%d" % w.cfg_id), "batch": w.batch,
             "steps": w.steps, "top_k": w.top_k, "seq_len": w.seq_len, "hot_buffer": w.hot_buffer,
@@ -230,6 +319,8 @@ def main():
     w = W.WORKLOADS[args.config]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.compare_sequential:
+        return run_compare_sequential(args, w)
 
     import torch
     rank, world, local = dist_env()

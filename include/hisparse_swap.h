@@ -200,6 +200,27 @@ int hs_export_request_state(hs_state* st, int32_t layer_id, int32_t request, int
                             int32_t* ep_host, int32_t* phys_host, int32_t* ctrl_host,
                             int64_t* bank_host, void* stream);
 
+/* Deferred-copy mode of the miss-plan protocol (the multi-step swap report,
+ * sections 实现拆解 item 2 and 风险与影响: the miss_src / miss_dst /
+ * miss_count plan lets the row copies be replayed by a prefetch path).
+ * When `defer` is non-zero, later hs_swap_in calls on this handle must be
+ * given the three miss-plan outputs and do not copy rows: they resolve
+ * locations and commit the policy state only.  The caller then runs
+ * hs_copy_planned with that plan, on any stream, ordered after the call and
+ * before (a) anything that reads the returned rows and (b) the next
+ * hs_swap_in on the same layer (whose scratch rows may be the same).
+ * 0 restores copying inside hs_swap_in.  Host only. */
+int hs_set_defer_copy(hs_state* st, int32_t defer);
+
+/* Copies the rows of a recorded miss plan: for batch row b and j <
+ * miss_count[b], host row miss_src[b, j] of layer `layer_id`'s pool to
+ * device row miss_dst[b, j] of its device buffer (W bytes each).  The plan
+ * is exactly what hs_swap_in wrote ([batch, C] with C = max_steps * top_k).
+ * Asynchronous on `stream`. */
+int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
+                    const int64_t* miss_dst_dev, const int32_t* miss_count_dev, int32_t batch,
+                    void* stream);
+
 /* Profiling: when `event_host` (a cudaEvent_t) is non-NULL, every later
  * hs_swap_in on this handle records it on its stream between the gather
  * kernel and the commit + copy kernel, and launches the latter without

@@ -88,6 +88,8 @@ def _declare(lib) -> None:
         "hs_export_request_state": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                                    _vp]),
         "hs_set_phase_event": (ctypes.c_int, [_vp, _vp]),
+        "hs_set_defer_copy": (ctypes.c_int, [_vp, _i32]),
+        "hs_copy_planned": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
         "hs_set_copy_ctas": (ctypes.c_int, [_vp, _i32]),
         "hs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "hs_version": (_i32, []),
@@ -302,3 +304,17 @@ def hs_set_phase_event(handle: StateHandle, event=None) -> None:
 
 def hs_set_copy_ctas(handle: StateHandle, copy_ctas: int) -> None:
     _check(load_library().hs_set_copy_ctas(handle.ptr, copy_ctas), "hs_set_copy_ctas")
+
+
+def hs_set_defer_copy(handle: StateHandle, defer: bool) -> None:
+    _check(load_library().hs_set_defer_copy(handle.ptr, 1 if defer else 0), "hs_set_defer_copy")
+
+
+def hs_copy_planned(handle: StateHandle, layer_id: int, miss_src, miss_dst, miss_count,
+                    stream=None) -> None:
+    import torch
+    rc = load_library().hs_copy_planned(
+        handle.ptr, layer_id, _dptr(miss_src, torch.int64, "miss_src"),
+        _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
+        miss_count.numel(), _stream_ptr(stream))
+    _check(rc, "hs_copy_planned")

@@ -22,6 +22,7 @@ struct hs_state {
     int num_sms;
     int copy_ctas;
     cudaEvent_t phase_event;  // profiling split between the two kernels, or null
+    int defer_copy;           // 1: hs_swap_in records the miss plan but copies nothing
 };
 
 namespace hs {
@@ -207,6 +208,7 @@ int hs_create_state(const hs_config* cfg, void* const* host_pool_host, void* con
     }
     st->copy_ctas = 2 * st->num_sms;
     st->phase_event = nullptr;
+    st->defer_copy = 0;
     int pageable_ok = 0;
     cudaDeviceGetAttribute(&pageable_ok, cudaDevAttrPageableMemoryAccess, st->device);
     cudaGetLastError();
@@ -256,6 +258,7 @@ int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t*
     const int plan = (miss_src_dev != nullptr) + (miss_dst_dev != nullptr) +
                      (miss_count_dev != nullptr);
     if (plan != 0 && plan != 3) return HS_ERR_INVALID_ARG;
+    if (st->defer_copy && plan == 0) return HS_ERR_INVALID_ARG;
     if (batch == 0) return HS_OK;
     if (!req_pool_indices_dev || !seq_lens_dev || !topk_dev || !device_locs_dev)
         return HS_ERR_INVALID_ARG;
@@ -279,9 +282,34 @@ int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_gather(a, s) != cudaSuccess) return HS_ERR_CUDA;
     if (st->phase_event && cudaEventRecord(st->phase_event, s) != cudaSuccess) return HS_ERR_CUDA;
-    if (launch_commit_copy(a, st->copy_ctas, st->phase_event == nullptr, s) != cudaSuccess)
+    const int copy_ctas = st->defer_copy ? 0 : st->copy_ctas;
+    if (launch_commit_copy(a, copy_ctas, st->phase_event == nullptr, s) != cudaSuccess)
         return HS_ERR_CUDA;
     return HS_OK;
+}
+
+int hs_set_defer_copy(hs_state* st, int32_t defer) {
+    if (!st) return HS_ERR_INVALID_ARG;
+    st->defer_copy = defer ? 1 : 0;
+    return HS_OK;
+}
+
+int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
+                    const int64_t* miss_dst_dev, const int32_t* miss_count_dev, int32_t batch,
+                    void* stream) {
+    if (!st) return HS_ERR_INVALID_ARG;
+    const Dims& d = st->d;
+    if (layer_id < 0 || layer_id >= d.layers || batch < 0 || batch > d.B_max)
+        return HS_ERR_INVALID_ARG;
+    if (batch == 0) return HS_OK;
+    if (!miss_src_dev || !miss_dst_dev || !miss_count_dev) return HS_ERR_INVALID_ARG;
+    return launch_planned_copy(reinterpret_cast<const long long*>(miss_src_dev),
+                               reinterpret_cast<const long long*>(miss_dst_dev), miss_count_dev,
+                               batch, d.C, d.W, st->host_pool_dev[layer_id],
+                               st->device_kv[layer_id], st->copy_ctas,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HS_OK
+               : HS_ERR_CUDA;
 }
 
 int hs_set_phase_event(hs_state* st, void* event_host) {

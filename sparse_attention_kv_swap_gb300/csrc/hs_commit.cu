@@ -308,40 +308,70 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
     }
 }
 
-__device__ void copy_rows(const SwapArgs& a, int cta, int ncta, int* pre) {
+// Where a unique miss's row comes from and goes to: the gather's workspace
+// lists (token -> host row of request q) ...
+struct WorkspaceRows {
+    const int32_t* cnt;
+    const int32_t* miss_tok;
+    const int32_t* miss_dst;
+    int32_t L, C;
+    __device__ int count(int b) const { return cnt[(long long)b * kCntWords + CNT_U]; }
+    __device__ void rows(int b, int j, long long* src, long long* dst) const {
+        const long long wi = (long long)b * C + j;
+        *src = (long long)cnt[(long long)b * kCntWords + CNT_Q] * L + miss_tok[wi];
+        *dst = miss_dst[wi];
+    }
+};
+
+// ... or a recorded miss plan (host row, device row, count per batch row).
+struct RecordedRows {
+    const long long* src;
+    const long long* dst;
+    const int32_t* count_;
+    int32_t C;
+    __device__ int count(int b) const { return count_[b]; }
+    __device__ void rows(int b, int j, long long* s, long long* d) const {
+        *s = src[(long long)b * C + j];
+        *d = dst[(long long)b * C + j];
+    }
+};
+
+// Copies every listed row (W bytes) from the host pool to the device buffer.
+// The rows of all batch rows are flattened; CTA `cta` of `ncta` takes one
+// contiguous span of 16-byte pieces, consecutive threads on consecutive
+// pieces, each thread issuing kCopyUnroll loads before its stores.
+template <typename Rows>
+__device__ void copy_rows(const Rows& plan, int B, int W, const uint8_t* pool, uint8_t* kv,
+                          int cta, int ncta, int* pre) {
     __shared__ int s_tmp[33];
-    const Dims& d = a.d;
     const int tid = threadIdx.x, BD = blockDim.x;
-    const int B = a.B;
-    // Exclusive prefix of the unique-miss counts over the batch rows.
+    // Exclusive prefix of the per-row counts over the batch rows.
     const int per = (B + BD - 1) / BD;
     const int b0 = tid * per, b1 = min(B, b0 + per);
     int sum = 0;
-    for (int b = b0; b < b1; ++b) sum += a.ws.cnt[(long long)b * kCntWords + CNT_U];
+    for (int b = b0; b < b1; ++b) sum += plan.count(b);
     int total;
     int run = block_exclusive_scan(sum, s_tmp, &total);
     for (int b = b0; b < b1; ++b) {
         pre[b] = run;
-        run += a.ws.cnt[(long long)b * kCntWords + CNT_U];
+        run += plan.count(b);
     }
     if (tid == 0) pre[B] = total;
     __syncthreads();
     if (total == 0) return;
 
-    const int nv = d.W >> 4;  // 16-byte pieces per row
+    const int nv = W >> 4;  // 16-byte pieces per row
     const long long chunks = (long long)total * nv;
     const long long span = (chunks + ncta - 1) / ncta;
     const long long c0 = (long long)cta * span;
     const long long c1 = min(chunks, c0 + span);
-    const uint8_t* pool = a.lv.host_pool;
-    uint8_t* kv = a.lv.device_kv;
     for (long long g = c0; g < c1; g += (long long)BD * kCopyUnroll) {
         uint4 v[kCopyUnroll];
-        int drow[kCopyUnroll];  // destination row of each piece, -1 if none
+        long long dst[kCopyUnroll];  // destination byte offset of each piece, -1 if none
 #pragma unroll
         for (int u = 0; u < kCopyUnroll; ++u) {
             const long long c = g + (long long)u * BD + tid;
-            drow[u] = -1;
+            dst[u] = -1;
             if (c < c1) {
                 const int row = (int)(c / nv);
                 const int piece = (int)(c - (long long)row * nv);
@@ -351,31 +381,36 @@ __device__ void copy_rows(const SwapArgs& a, int cta, int ncta, int* pre) {
                     if (pre[mid] <= row) lo = mid;
                     else hi = mid;
                 }
-                const long long wi = (long long)lo * d.C + (row - pre[lo]);
-                const int q = a.ws.cnt[(long long)lo * kCntWords + CNT_Q];
-                const long long src =
-                    ((long long)q * d.L + a.ws.miss_tok[wi]) * d.W + ((long long)piece << 4);
-                drow[u] = a.ws.miss_dst[wi];
-                v[u] = ld_stream_v4(pool + src);
+                long long srow, drow;
+                plan.rows(lo, row - pre[lo], &srow, &drow);
+                dst[u] = drow * W + ((long long)piece << 4);
+                v[u] = ld_stream_v4(pool + srow * W + ((long long)piece << 4));
             }
         }
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
-            if (drow[u] < 0) continue;
-            const long long c = g + (long long)u * BD + tid;
-            const long long piece = c - (c / nv) * nv;
-            st_v4(kv + (long long)drow[u] * d.W + (piece << 4), v[u]);
-        }
+        for (int u = 0; u < kCopyUnroll; ++u)
+            if (dst[u] >= 0) st_v4(kv + dst[u], v[u]);
     }
 }
 
 __global__ void __launch_bounds__(kBlock, 2) commit_copy_kernel(const SwapArgs a, int copy_ctas) {
     extern __shared__ __align__(16) unsigned char smem[];
     pdl_wait();  // the gather grid's results are visible after this
-    if ((int)blockIdx.x < a.B)
+    if ((int)blockIdx.x < a.B) {
         commit_request(a, blockIdx.x, reinterpret_cast<unsigned*>(smem));
-    else
-        copy_rows(a, blockIdx.x - a.B, copy_ctas, reinterpret_cast<int*>(smem));
+    } else {
+        const WorkspaceRows plan{a.ws.cnt, a.ws.miss_tok, a.ws.miss_dst, a.d.L, a.d.C};
+        copy_rows(plan, a.B, a.d.W, a.lv.host_pool, a.lv.device_kv, blockIdx.x - a.B, copy_ctas,
+                  reinterpret_cast<int*>(smem));
+    }
+}
+
+// Replays a recorded miss plan (the deferred copy of a swap-in call).
+__global__ void __launch_bounds__(kBlock, 2) planned_copy_kernel(const RecordedRows plan, int B,
+                                                                  int W, const uint8_t* pool,
+                                                                  uint8_t* kv) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    copy_rows(plan, B, W, pool, kv, blockIdx.x, gridDim.x, reinterpret_cast<int*>(smem));
 }
 
 }  // namespace
@@ -402,6 +437,18 @@ cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaS
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, commit_copy_kernel, a, copy_ctas);
+}
+
+cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
+                                int32_t B, int32_t C, int32_t W, const uint8_t* pool,
+                                uint8_t* kv, int ctas, cudaStream_t s) {
+    static int cached = 48 * 1024;
+    const size_t smem = (size_t)(B + 1) * 4;
+    cudaError_t e = ensure_smem(planned_copy_kernel, smem, &cached);
+    if (e != cudaSuccess) return e;
+    const RecordedRows plan{src, dst, count, C};
+    planned_copy_kernel<<<ctas, kBlock, smem, s>>>(plan, B, W, pool, kv);
+    return cudaGetLastError();
 }
 
 }  // namespace hs

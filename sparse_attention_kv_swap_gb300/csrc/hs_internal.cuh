@@ -116,6 +116,9 @@ size_t gather_smem_bytes(int entries, int* dedup_size);
 cudaError_t launch_gather(const SwapArgs& a, cudaStream_t s);
 size_t commit_smem_bytes(const Dims& d);
 cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s);
+cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
+                                int32_t B, int32_t C, int32_t W, const uint8_t* pool,
+                                uint8_t* kv, int ctas, cudaStream_t s);
 cudaError_t launch_reset(const Dims& d, uint8_t* state, const int32_t* rpi, int32_t n,
                          cudaStream_t s);
 cudaError_t launch_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t B,

@@ -34,7 +34,8 @@ def bank_consistent(st: dict) -> Optional[str]:
 
 class ParityRun:
     def __init__(self, R: int, L: int, width: int, H: int, K: int, S_max: int, layers: int = 1,
-                 max_batch: Optional[int] = None, pools=None):
+                 max_batch: Optional[int] = None, pools=None, deferred: bool = False):
+        self.deferred = deferred
         import sparse_attention_kv_swap_gb300 as pkg
         from oracle import Oracle
         from sparse_attention_kv_swap_gb300.cache import SwapInCache
@@ -52,6 +53,8 @@ class ParityRun:
         self.cache = SwapInCache(cfg, host_pools=pools)
         for t in self.cache.device_kv:
             t.zero_()
+        if deferred:
+            pkg.hs_set_defer_copy(self.cache.handle, True)
         self.oracle = Oracle(R, L, width, H, K, S_max, layers)
         self.mirror = [np.zeros((R * (H + self.C), width), dtype=np.uint8) for _ in range(layers)]
         self.calls = 0
@@ -67,7 +70,18 @@ class ParityRun:
         seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
         before = {int(q): self.gpu_state(layer, int(q)) for q in rpi} if properties else None
         out = self.cache.swap_in(torch.from_numpy(rpi).cuda(), torch.from_numpy(seq_lens).cuda(),
-                                 torch.from_numpy(topk).cuda(), layer, stats=True, plan=plan)
+                                 torch.from_numpy(topk).cuda(), layer, stats=True,
+                                 plan=plan or self.deferred)
+        if self.deferred:
+            # the rows arrive only when the recorded plan is replayed, here on
+            # a second stream ordered after the call
+            import sparse_attention_kv_swap_gb300 as pkg
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            pkg.hs_copy_planned(self.cache.handle, layer, out["miss_src"], out["miss_dst"],
+                                out["miss_count"], stream=side)
+            torch.cuda.current_stream().wait_stream(side)
+            plan = True
         ref = self.oracle.swap_in(layer, self.pools[layer].numpy(), self.mirror[layer], rpi,
                                   seq_lens, topk, want_plan=plan, num_threads=threads)
         torch.cuda.synchronize()

@@ -70,6 +70,22 @@ def test_miss_plan_matches():
         run.call(topk, rpi, sl, plan=True)
 
 
+def test_deferred_copy_replays_plan_exactly():
+    """Deferred mode: the call copies nothing; replaying its miss plan on
+    another stream gives the same rows, locations and state as the oracle."""
+    rng = np.random.default_rng(10)
+    run = ParityRun(4, 3000, W.ROW_BYTES, 200, 300, 4, deferred=True)
+    for topk, rpi, sl in _rand_calls(rng, 4, 3000, 300, 4, 4, 6):
+        run.call(topk, rpi, sl)
+    import pytest as _pt
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    with _pt.raises(pkg.HsError):  # deferred mode needs the plan outputs
+        i32 = dict(dtype=torch.int32, device="cuda")
+        pkg.hs_swap_in(run.cache.handle, torch.tensor([0], **i32), torch.tensor([5], **i32),
+                       torch.zeros((1, 1, 300), **i32), 0, torch.empty((1, 1, 300), **i32))
+
+
 def test_reset_requests_matches():
     import torch
     rng = np.random.default_rng(11)
