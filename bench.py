@@ -415,6 +415,8 @@ def main():
     e_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
     e_m = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
     e_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
+    for e in e_m:  # torch creates the CUDA event at its first record
+        e.record(s)
     pbase = base + K
     for k in range(n_phase):
         flush.fill_(k & 0xFF)
