@@ -233,6 +233,40 @@ int hs_set_phase_event(hs_state* st, void* event_host);
  * count); otherwise 1..65535.  Host only. */
 int hs_set_copy_ctas(hs_state* st, int32_t copy_ctas);
 
+/* Size of the per-call scratch array of hs_swap_in_noalloc (16 MiB). */
+#define HS_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* hs_swap_in for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point.
+ *
+ * Some callers cannot call cudaMalloc, or any routine that allocates, on the
+ * path that issues swap-ins.  Examples: a plugin that a serving runtime hands
+ * only its input and output tensors, and code that must not allocate while a
+ * stream is being captured.  This call takes the same arguments as
+ * hs_swap_in and gives the same results.  Its per-call scratch (miss lists,
+ * victim and admission lists, per-request counters) lives in one file-scope
+ * device array of HS_NOALLOC_SCRATCH_BYTES, not in the handle's workspace.
+ * Every GPU that loads the library holds that array until the process exits.
+ * The call allocates nothing.
+ *   - A call needs 5 * align256(4 * batch * C) + align256(64 * batch) bytes
+ *     (C = max_steps * top_k).  A larger call returns HS_ERR_UNSUPPORTED
+ *     before any launch; e.g. batch 64 with C = 8192 needs 10.5 MB.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current.  Make that first
+ *     call before any stream capture.
+ *   - All calls share the array, and it keeps the last call's contents.
+ *     Nothing in it needs clearing: a call writes every element before it
+ *     reads it.  Calls whose kernels can overlap on the GPU (other streams,
+ *     other handles, no ordering between them) race on the array: order them.
+ *   - Device status flags still go to the handle (read with hs_get_status).
+ * Everything else (state, host pool, device buffer, deferred-copy and
+ * phase-event settings) is the handle's, as for hs_swap_in. */
+int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_dev,
+                       const int32_t* seq_lens_dev, const int32_t* topk_dev, int32_t batch,
+                       int32_t num_steps, int32_t layer_id, int32_t* device_locs_dev,
+                       int32_t* stats_dev, int64_t* miss_src_dev, int64_t* miss_dst_dev,
+                       int32_t* miss_count_dev, void* stream);
+
 /* Static string for a return code. */
 const char* hs_status_string(int code);
 

@@ -87,6 +87,8 @@ def _declare(lib) -> None:
         "hs_get_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
         "hs_export_request_state": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                                    _vp]),
+        "hs_swap_in_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
+                                              _vp, _vp, _vp, _vp]),
         "hs_set_phase_event": (ctypes.c_int, [_vp, _vp]),
         "hs_set_defer_copy": (ctypes.c_int, [_vp, _i32]),
         "hs_copy_planned": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
@@ -318,3 +320,20 @@ def hs_copy_planned(handle: StateHandle, layer_id: int, miss_src, miss_dst, miss
         _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
         miss_count.numel(), _stream_ptr(stream))
     _check(rc, "hs_copy_planned")
+
+
+def hs_swap_in_noalloc(handle: StateHandle, req_pool_indices, seq_lens, topk, layer_id: int,
+                       device_locs, stats=None, miss_src=None, miss_dst=None, miss_count=None,
+                       stream=None) -> None:
+    """hs_swap_in whose per-call scratch is the library's fixed device array
+    (for callers that cannot allocate device memory); see the C header."""
+    import torch
+    B, S, K = topk.shape
+    rc = load_library().hs_swap_in_noalloc(
+        handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
+        _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
+        layer_id, _dptr(device_locs, torch.int32, "device_locs"),
+        _dptr(stats, torch.int32, "stats"), _dptr(miss_src, torch.int64, "miss_src"),
+        _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
+        _stream_ptr(stream))
+    _check(rc, "hs_swap_in_noalloc")

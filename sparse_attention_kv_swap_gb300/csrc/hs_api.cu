@@ -9,22 +9,6 @@
 
 #include "hs_internal.cuh"
 
-struct hs_state {
-    hs_config cfg;
-    hs::Dims d;
-    hs::StateLayout sl;
-    hs::WorkspaceLayout wl;
-    uint8_t* state;
-    uint8_t* ws;
-    std::vector<const uint8_t*> host_pool_dev;  // device mapping of each layer's pool
-    std::vector<uint8_t*> device_kv;
-    int device;
-    int num_sms;
-    int copy_ctas;
-    cudaEvent_t phase_event;  // profiling split between the two kernels, or null
-    int defer_copy;           // 1: hs_swap_in records the miss plan but copies nothing
-};
-
 namespace hs {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -192,3 +192,22 @@ __device__ __forceinline__ int block_sum(int x, int* tmp) {
 #endif  // __CUDACC__
 
 }  // namespace hs
+
+#include <vector>
+
+// The host handle behind the C ABI's opaque hs_state.
+struct hs_state {
+    hs_config cfg;
+    hs::Dims d;
+    hs::StateLayout sl;
+    hs::WorkspaceLayout wl;
+    uint8_t* state;
+    uint8_t* ws;
+    std::vector<const uint8_t*> host_pool_dev;  // device mapping of each layer's pool
+    std::vector<uint8_t*> device_kv;
+    int device;
+    int num_sms;
+    int copy_ctas;
+    cudaEvent_t phase_event;  // profiling split between the two kernels, or null
+    int defer_copy;           // 1: hs_swap_in records the miss plan but copies nothing
+};

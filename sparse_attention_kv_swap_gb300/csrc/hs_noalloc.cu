@@ -1,0 +1,116 @@
+// hs_swap_in_noalloc: the swap-in for callers that cannot allocate device
+// memory.  It has no counterpart in the pages this library follows.
+//
+// Some callers cannot call cudaMalloc (or any routine that allocates) on the
+// path that issues swap-ins.  Examples are a plugin that a serving runtime
+// hands only its input and output tensors, and code that must not allocate
+// while a stream is being captured.  This entry point behaves exactly like
+// hs_swap_in, but the per-call scratch of the two kernels (miss lists, victim
+// and admission lists, per-request counters) lives in one file-scope device
+// array of fixed size, not in the handle's workspace.  Every GPU that loads
+// the library holds the array until the process exits.
+#include <mutex>
+
+#include "hs_internal.cuh"
+
+namespace hs {
+namespace {
+
+// The shared per-call scratch.  In host code this name is only a host-side
+// stand-in; kernels get its device address from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HS_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Device address of the scratch array on `device` (the current device),
+// looked up once per device.
+cudaError_t scratch_address(int device, unsigned char** out) {
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_addr[device]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[device] = p;
+    }
+    *out = static_cast<unsigned char*>(g_scratch_addr[device]);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+// Bytes of per-call scratch a call with `batch` rows needs (same regions as
+// the handle's workspace, sized for `batch` rather than max_batch).
+static size_t noalloc_bytes(const Dims& d, int batch) {
+    const size_t bc = align256((size_t)batch * d.C * 4);
+    return 5 * bc + align256((size_t)batch * kCntWords * 4);
+}
+
+}  // namespace hs
+
+using namespace hs;
+
+extern "C" int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_dev,
+                                  const int32_t* seq_lens_dev, const int32_t* topk_dev,
+                                  int32_t batch, int32_t num_steps, int32_t layer_id,
+                                  int32_t* device_locs_dev, int32_t* stats_dev,
+                                  int64_t* miss_src_dev, int64_t* miss_dst_dev,
+                                  int32_t* miss_count_dev, void* stream) {
+    if (!st) return HS_ERR_INVALID_ARG;
+    const Dims& d = st->d;
+    if (batch < 0 || batch > d.B_max) return HS_ERR_INVALID_ARG;
+    if (num_steps < 1 || num_steps > d.S_max) return HS_ERR_INVALID_ARG;
+    if (layer_id < 0 || layer_id >= d.layers) return HS_ERR_INVALID_ARG;
+    const int plan = (miss_src_dev != nullptr) + (miss_dst_dev != nullptr) +
+                     (miss_count_dev != nullptr);
+    if (plan != 0 && plan != 3) return HS_ERR_INVALID_ARG;
+    if (st->defer_copy && plan == 0) return HS_ERR_INVALID_ARG;
+    if (noalloc_bytes(d, batch) > HS_NOALLOC_SCRATCH_BYTES) return HS_ERR_UNSUPPORTED;
+    if (batch == 0) return HS_OK;
+    if (!req_pool_indices_dev || !seq_lens_dev || !topk_dev || !device_locs_dev)
+        return HS_ERR_INVALID_ARG;
+
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return HS_ERR_CUDA;
+    unsigned char* scratch = nullptr;
+    if (scratch_address(device, &scratch) != cudaSuccess) return HS_ERR_CUDA;
+
+    // Carve the scratch like the workspace; the status word stays the
+    // handle's, so hs_get_status reports this call's device flags too.
+    const size_t bc = align256((size_t)batch * d.C * 4);
+    Workspace ws;
+    ws.miss_tok = reinterpret_cast<int32_t*>(scratch);
+    ws.miss_last = reinterpret_cast<int32_t*>(scratch + bc);
+    ws.miss_dst = reinterpret_cast<int32_t*>(scratch + 2 * bc);
+    ws.vict = reinterpret_cast<int32_t*>(scratch + 3 * bc);
+    ws.adm = reinterpret_cast<int32_t*>(scratch + 4 * bc);
+    ws.cnt = reinterpret_cast<int32_t*>(scratch + 5 * bc);
+    ws.status = reinterpret_cast<uint32_t*>(st->ws + st->wl.status);
+
+    SwapArgs a = {};
+    a.d = d;
+    a.lv = layer_view(d, st->state, layer_id, st->host_pool_dev[layer_id],
+                      st->device_kv[layer_id]);
+    a.ws = ws;
+    a.rpi = req_pool_indices_dev;
+    a.seq_lens = seq_lens_dev;
+    a.topk = topk_dev;
+    a.B = batch;
+    a.S = num_steps;
+    a.locs = device_locs_dev;
+    a.stats = stats_dev;
+    a.plan_src = reinterpret_cast<long long*>(miss_src_dev);
+    a.plan_dst = reinterpret_cast<long long*>(miss_dst_dev);
+    a.plan_count = miss_count_dev;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_gather(a, s) != cudaSuccess) return HS_ERR_CUDA;
+    if (st->phase_event && cudaEventRecord(st->phase_event, s) != cudaSuccess) return HS_ERR_CUDA;
+    const int copy_ctas = st->defer_copy ? 0 : st->copy_ctas;
+    if (launch_commit_copy(a, copy_ctas, st->phase_event == nullptr, s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
