@@ -144,6 +144,13 @@ def measure_h2d_peak(torch, dev, nbytes=256 << 20, reps=20):
     return best
 
 
+def gate(torch, steps):
+    """Hold the stream with a short device-side sleep so that the host can
+    queue every step before the first one runs: the per-step events then see
+    GPU time only, not host launch latency."""
+    torch.cuda._sleep(int(2e6 * (5 + 0.25 * steps)))  # ~2e6 cycles per ms
+
+
 def read_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -218,6 +225,45 @@ def run_reference(args, w):
     return 0
 
 
+def copy_ceiling(torch, pkg, cache, w, dev, flush, rows_per_request, reps=10):
+    """Host-link ceiling of the library's row copy: replays synthetic miss
+    plans with hs_copy_planned (same kernel code as the swap-in's copy) for
+    (a) consecutive host rows and (b) random host rows, the latter with as many
+    rows per request as a measured step.  Writes device rows, so it runs after
+    every other measurement."""
+    Bn, C, H, L, Wr = w.batch, w.steps * w.top_k, w.hot_buffer, w.seq_len, w.row_bytes
+    rng = np.random.default_rng(5)
+    out = {}
+    for kind, n in (("consecutive_rows", C), ("random_rows", max(1, int(rows_per_request)))):
+        n = min(n, C)
+        src = np.zeros((Bn, C), np.int64)
+        dst = np.zeros((Bn, C), np.int64)
+        for b in range(Bn):
+            if kind == "consecutive_rows":
+                toks = np.arange(n) + rng.integers(0, L - n + 1)
+            else:
+                toks = rng.choice(L, size=n, replace=False)
+            src[b, :n] = b * L + toks
+            dst[b, :n] = b * (H + C) + H + np.arange(n)
+        cnt = torch.full((Bn,), n, dtype=torch.int32, device=dev)
+        s_t, d_t = torch.from_numpy(src).to(dev), torch.from_numpy(dst).to(dev)
+        times = []
+        for r in range(reps + 2):
+            flush.fill_(r & 0xFF)
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            pkg.hs_copy_planned(cache.handle, 0, s_t, d_t, cnt)
+            b_.record()
+            b_.synchronize()
+            if r >= 2:
+                times.append(a.elapsed_time(b_))
+        ms = statistics.median(times)
+        nbytes = Bn * n * Wr
+        out[kind] = {"rows": Bn * n, "mb": nbytes / 1e6, "ms": ms,
+                     "gbs": nbytes / (ms * 1e-3) / 1e9}
+    return out
+
+
 def run_compare_sequential(args, w):
     """Multi-step swap (one S-step call) against sequential per-step swap (S
     single-step calls) on the same index stream, each captured as a CUDA
@@ -282,9 +328,10 @@ def run_compare_sequential(args, w):
             flush.fill_(i & 0xFF)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
-            a.record(stream)
-            g.replay()
-            b.record(stream)
+            with torch.cuda.stream(stream):  # replay runs on the current stream
+                a.record(stream)
+                g.replay()
+                b.record(stream)
             b.synchronize()
             if timed:
                 acc.append(a.elapsed_time(b))
@@ -391,6 +438,7 @@ def main():
     torch.cuda.synchronize()
     t_wall0 = time.time()
     base = PREROLL_CALLS + Wm
+    gate(torch, K)
     for k in range(K):
         flush.fill_(k & 0xFF)
         ev[k][0].record(s)
@@ -418,6 +466,7 @@ def main():
     for e in e_m:  # torch creates the CUDA event at its first record
         e.record(s)
     pbase = base + K
+    gate(torch, n_phase)
     for k in range(n_phase):
         flush.fill_(k & 0xFF)
         pkg.hs_set_phase_event(cache.handle, e_m[k])
@@ -443,6 +492,7 @@ def main():
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n_e2e)]
     torch.cuda.synchronize()
+    gate(torch, n_e2e)
     for k in range(n_e2e):
         flush.fill_(k & 0xFF)
         e2e_ev[k][0].record(s)
@@ -465,6 +515,8 @@ def main():
     rc, flags = cache.status()
     if flags:
         raise RuntimeError("device status flags %#x after the timed region" % flags)
+    ceiling = copy_ceiling(torch, pkg, cache, w, dev, flush,
+                           float(stats[base:base + K, :, 3].float().mean()))
 
     # ---- roofline bookkeeping (algorithmic bytes) ----
     U_phase = st_phase[:, :, 3].sum(axis=1).astype(np.float64)
@@ -506,6 +558,7 @@ def main():
             "miss_copy_mb_per_step": float(np.mean(U_timed)) * w.row_bytes / 1e6,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
         },
+        "copy_ceiling": ceiling,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

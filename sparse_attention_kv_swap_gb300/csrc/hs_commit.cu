@@ -177,34 +177,45 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
         int need = m;
         unsigned thr = 0u;
         if (bits > 0) thr = radix_select(keys, H, m, bits, s_hist, s_sel, &need);
-        // Thread-contiguous segments keep slot order for the scans.
-        const int seg = (H + BD - 1) / BD;
-        const int v0 = tid * seg, v1 = min(H, v0 + seg);
+        // Each warp owns a contiguous chunk of slots, read lane by lane, so
+        // ballots keep ascending slot order without shared-memory conflicts.
+        const int lane = tid & 31, warp = tid >> 5, nw = BD >> 5;
+        const int chunk = ((H + nw - 1) / nw + 31) & ~31;
+        const int w0 = warp * chunk, w1 = min(H, w0 + chunk);
         int eq = 0;
-        for (int v = v0; v < v1; ++v) eq += (keys[v] == thr);
+        for (int v0 = w0; v0 < w1; v0 += 32) {
+            const int v = v0 + lane;
+            eq += __popc(__ballot_sync(0xffffffffu, v < w1 && keys[v] == thr));
+        }
         int eq_total;
-        int eq_before = block_exclusive_scan(eq, s_tmp, &eq_total);
+        const int eq_before = block_exclusive_scan(lane == 0 ? eq : 0, s_tmp, &eq_total);
+        const int eq_w = __shfl_sync(0xffffffffu, eq_before, 0);
         int nv = 0;
         {
-            int er = eq_before;
-            for (int v = v0; v < v1; ++v) {
-                const unsigned k = keys[v];
-                if (k == kHitKey) continue;
-                if (k < thr) ++nv;
-                else if (k == thr && er++ < need) ++nv;
+            int er = eq_w;
+            for (int v0 = w0; v0 < w1; v0 += 32) {
+                const int v = v0 + lane;
+                const unsigned k = v < w1 ? keys[v] : kHitKey;
+                const unsigned em = __ballot_sync(0xffffffffu, k == thr);
+                const bool take = k < thr || (k == thr && er + __popc(em & lanemask_lt()) < need);
+                nv += __popc(__ballot_sync(0xffffffffu, take));
+                er += __popc(em);
             }
         }
         int nv_total;
-        int vpos = block_exclusive_scan(nv, s_tmp, &nv_total);
+        const int v_before = block_exclusive_scan(lane == 0 ? nv : 0, s_tmp, &nv_total);
         {
-            int er = eq_before;
-            for (int v = v0; v < v1; ++v) {
-                const unsigned k = keys[v];
-                if (k == kHitKey) continue;
-                bool take = false;
-                if (k < thr) take = true;
-                else if (k == thr && er++ < need) take = true;
-                if (take) vict[vpos++] = v;
+            int er = eq_w;
+            int vpos = __shfl_sync(0xffffffffu, v_before, 0);
+            for (int v0 = w0; v0 < w1; v0 += 32) {
+                const int v = v0 + lane;
+                const unsigned k = v < w1 ? keys[v] : kHitKey;
+                const unsigned em = __ballot_sync(0xffffffffu, k == thr);
+                const bool take = k < thr || (k == thr && er + __popc(em & lanemask_lt()) < need);
+                const unsigned tm = __ballot_sync(0xffffffffu, take);
+                if (take) vict[vpos + __popc(tm & lanemask_lt())] = v;
+                vpos += __popc(tm);
+                er += __popc(em);
             }
         }
         // ---- admitted misses ---------------------------------------------------
@@ -212,7 +223,14 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
             const int* last = a.ws.miss_last + wbase;
             if (tid < 8) s_misc[tid] = 0;
             __syncthreads();
-            for (int j = tid; j < U; j += BD) atomicAdd(&s_misc[last[j]], 1);
+            for (int x0 = tid & ~31; x0 < U; x0 += BD) {  // per-step counts, one add per warp
+                const int j = x0 + lane;
+                const int l = j < U ? last[j] : -1;
+                for (int st = 0; st < a.S; ++st) {
+                    const int c = __popc(__ballot_sync(0xffffffffu, l == st));
+                    if (lane == 0 && c) atomicAdd(&s_misc[st], c);
+                }
+            }
             __syncthreads();
             // threshold step: walk from the latest step down
             int s_thr = 0, need_s = m, acc = 0;
@@ -224,25 +242,45 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
                 }
                 acc += s_misc[s];
             }
-            const int segj = (U + BD - 1) / BD;
-            const int j0 = tid * segj, j1 = min(U, j0 + segj);
+            const int cj = ((U + nw - 1) / nw + 31) & ~31;
+            const int j0 = warp * cj, j1 = min(U, j0 + cj);
             int eqs = 0;
-            for (int j = j0; j < j1; ++j) eqs += (last[j] == s_thr);
+            for (int x0 = j0; x0 < j1; x0 += 32) {
+                const int j = x0 + lane;
+                eqs += __popc(__ballot_sync(0xffffffffu, j < j1 && last[j] == s_thr));
+            }
             int eqs_total;
-            int er = block_exclusive_scan(eqs, s_tmp, &eqs_total);
+            const int es_before = block_exclusive_scan(lane == 0 ? eqs : 0, s_tmp, &eqs_total);
+            const int es_w = __shfl_sync(0xffffffffu, es_before, 0);
             int na = 0;
             {
-                int r = er;
-                for (int j = j0; j < j1; ++j) {
-                    const int l = last[j];
-                    if (l > s_thr || (l == s_thr && r++ < need_s)) ++na;
+                int er = es_w;
+                for (int x0 = j0; x0 < j1; x0 += 32) {
+                    const int j = x0 + lane;
+                    const int l = j < j1 ? last[j] : -1;
+                    const unsigned em = __ballot_sync(0xffffffffu, l == s_thr);
+                    const bool take =
+                        l > s_thr || (l == s_thr && er + __popc(em & lanemask_lt()) < need_s);
+                    na += __popc(__ballot_sync(0xffffffffu, take));
+                    er += __popc(em);
                 }
             }
             int na_total;
-            int apos = block_exclusive_scan(na, s_tmp, &na_total);
-            for (int j = j0; j < j1; ++j) {
-                const int l = last[j];
-                if (l > s_thr || (l == s_thr && er++ < need_s)) adm[apos++] = j;
+            const int a_before = block_exclusive_scan(lane == 0 ? na : 0, s_tmp, &na_total);
+            {
+                int er = es_w;
+                int apos = __shfl_sync(0xffffffffu, a_before, 0);
+                for (int x0 = j0; x0 < j1; x0 += 32) {
+                    const int j = x0 + lane;
+                    const int l = j < j1 ? last[j] : -1;
+                    const unsigned em = __ballot_sync(0xffffffffu, l == s_thr);
+                    const bool take =
+                        l > s_thr || (l == s_thr && er + __popc(em & lanemask_lt()) < need_s);
+                    const unsigned tm = __ballot_sync(0xffffffffu, take);
+                    if (take) adm[apos + __popc(tm & lanemask_lt())] = j;
+                    apos += __popc(tm);
+                    er += __popc(em);
+                }
             }
         }
         __syncthreads();

@@ -112,8 +112,9 @@ cudaError_t ensure_smem(F* kernel, size_t bytes, int* cached) {
 }
 
 // Launchers (each returns the launch's error code).
-size_t gather_smem_bytes(int entries, int* dedup_size);
-cudaError_t launch_gather(const SwapArgs& a, cudaStream_t s);
+int gather_cluster_size(int batch, int entries, int sms);
+size_t gather_smem_bytes(int entries, int cluster, int* dedup_size);
+cudaError_t launch_gather(const SwapArgs& a, int sms, cudaStream_t s);
 size_t commit_smem_bytes(const Dims& d);
 cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s);
 cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
