@@ -234,15 +234,22 @@ def copy_ceiling(torch, pkg, cache, w, dev, flush, rows_per_request, reps=10):
     Bn, C, H, L, Wr = w.batch, w.steps * w.top_k, w.hot_buffer, w.seq_len, w.row_bytes
     rng = np.random.default_rng(5)
     out = {}
-    for kind, n in (("consecutive_rows", C), ("random_rows", max(1, int(rows_per_request)))):
+    n_step = max(1, int(rows_per_request))
+    # rows whose host byte offset is a multiple of 128 (t * W % 128 == 0)
+    align = 128 // int(np.gcd(Wr, 128))
+    for kind, n in (("consecutive_rows", C), ("random_rows", n_step),
+                    ("random_rows_128B_aligned", n_step)):
         n = min(n, C)
         src = np.zeros((Bn, C), np.int64)
         dst = np.zeros((Bn, C), np.int64)
         for b in range(Bn):
             if kind == "consecutive_rows":
                 toks = np.arange(n) + rng.integers(0, L - n + 1)
-            else:
+            elif kind == "random_rows":
                 toks = rng.choice(L, size=n, replace=False)
+            else:
+                n = min(n, L // align)
+                toks = rng.choice(L // align, size=n, replace=False) * align
             src[b, :n] = b * L + toks
             dst[b, :n] = b * (H + C) + H + np.arange(n)
         cnt = torch.full((Bn,), n, dtype=torch.int32, device=dev)

@@ -48,6 +48,13 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v) {
                  : "memory");
 }
 
+// Non-binding prefetch of [p, p + bytes) into L2, one 128-byte line per thread.
+__device__ __forceinline__ void l2_prefetch(const void* p, size_t bytes) {
+    const char* c = static_cast<const char*>(p);
+    for (size_t off = (size_t)threadIdx.x * 128; off < bytes; off += (size_t)blockDim.x * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+}
+
 // Deletes token t from a request's hash bank (the entry must exist).
 __device__ void bank_delete(long long* bank, int shift, unsigned mask, int32_t t,
                             uint32_t* status) {
@@ -284,30 +291,32 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
             }
         }
         __syncthreads();
-        // ---- evict: the victims' old tokens leave the hash --------------------
-        for (int i = tid; i < m; i += BD) {
-            const int v = vict[i];
-            const int old = tok[v];
-            if (old >= 0) {
-                bank_delete(bank, d.hash_shift, hmask, old, a.ws.status);
-                ++evicted;
-            }
-        }
-        evicted = block_sum(evicted, s_tmp);  // barrier: all deletions done
-        // ---- rotate and admit --------------------------------------------------
+        // ---- evict, rotate and admit ------------------------------------------
+        // A pair's four loads are independent.  Deletions and insertions may
+        // interleave: a deletion only rewrites an entry that holds its own
+        // (live) key and an insertion only claims empty or deleted entries,
+        // so an insertion that probes past a live entry being deleted just
+        // lands further along its chain.
         int fresh = 0;
         const int32_t* mtok = a.ws.miss_tok + wbase;
         for (int i = tid; i < m; i += BD) {
             const int v = vict[i];
             const int j = (U > cap) ? adm[i] : i;
-            const int p = phys[v];
-            phys[v] = phys[H + j];
-            phys[H + j] = p;
+            const int old = tok[v];
+            const int pv = phys[v];
+            const int ps = phys[H + j];
             const int t = mtok[j];
+            phys[v] = ps;
+            phys[H + j] = pv;
             tok[v] = t;
             ep[v] = E;
+            if (old >= 0) {
+                bank_delete(bank, d.hash_shift, hmask, old, a.ws.status);
+                ++evicted;
+            }
             fresh += bank_insert(bank, d.hash_shift, hmask, t, v, a.ws.status);
         }
+        evicted = block_sum(evicted, s_tmp);
         fresh = block_sum(fresh, s_tmp);
         if (tid == 0) {
             s_misc[0] = ctrl[CTRL_USED] + fresh;
@@ -433,6 +442,18 @@ __device__ void copy_rows(const Rows& plan, int B, int W, const uint8_t* pool, u
 
 __global__ void __launch_bounds__(kBlock, 2) commit_copy_kernel(const SwapArgs a, int copy_ctas) {
     extern __shared__ __align__(16) unsigned char smem[];
+    if ((int)blockIdx.x < a.B) {
+        // Before the gather finishes: pull this request's policy state into
+        // L2 (a prefetch only; nothing is read before the wait below).
+        const int q = a.rpi[blockIdx.x];
+        if (q >= 0 && q < a.d.R) {
+            const Dims& d = a.d;
+            l2_prefetch(a.lv.ep + (long long)q * d.H, (size_t)d.H * 4);
+            l2_prefetch(a.lv.tok + (long long)q * d.H, (size_t)d.H * 4);
+            l2_prefetch(a.lv.phys + (long long)q * (d.H + d.C), (size_t)(d.H + d.C) * 4);
+            l2_prefetch(a.lv.bank + (long long)q * d.hash_size, (size_t)d.hash_size * 8);
+        }
+    }
     pdl_wait();  // the gather grid's results are visible after this
     if ((int)blockIdx.x < a.B) {
         commit_request(a, blockIdx.x, reinterpret_cast<unsigned*>(smem));

@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
     for (int i = tid; i < (TS >> 2); i += BD) smask[i] = 0u;
     if (tid < 3) s_cnt[tid] = 0;
     cluster.sync();  // every CTA of the cluster runs and its sub-table is empty
+    // Let the commit + copy kernel launch now: its CTAs warm L2 with their
+    // request's state while this grid works, and wait for this grid's
+    // completion before reading anything it writes.
+    pdl_trigger();
 
     // ---- 1. probe the hash bank (all first probes issued before any resolves)
     const long long* bank = a.lv.bank + (long long)(q_ok ? q : 0) * d.hash_size;
@@ -193,7 +197,6 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
             if (a.stats && tid < HS_NUM_STATS) a.stats[(long long)b * HS_NUM_STATS + tid] = 0;
             if (a.plan_count && tid == 0) a.plan_count[b] = 0;
         }
-        pdl_trigger();
         return;
     }
     const int E = s_epoch;
@@ -324,7 +327,6 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
         }
         if (a.plan_count) a.plan_count[b] = U;
     }
-    pdl_trigger();
 }
 
 template <int RMAX>
