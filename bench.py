@@ -144,6 +144,20 @@ def measure_h2d_peak(torch, dev, nbytes=256 << 20, reps=20):
     return best
 
 
+def max_over_ranks(torch, ms, world, device):
+    """The slowest rank's time (every rank holds its own replica)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(entries_per_replica, world, ms):
+    """Tokens resolved per second by all replicas together (weak scaling)."""
+    return entries_per_replica * world / (ms * 1e-3)
+
+
 def gate(torch, steps):
     """Hold the stream with a short device-side sleep so that the host can
     queue every step before the first one runs: the per-step events then see
@@ -446,11 +460,13 @@ def main():
     t_wall0 = time.time()
     base = PREROLL_CALLS + Wm
     gate(torch, K)
+    torch.cuda.nvtx.range_push("timed_steps")  # lets a profiler select these launches
     for k in range(K):
         flush.fill_(k & 0xFF)
         ev[k][0].record(s)
         step(base + k, topk_all[base + k])
         ev[k][1].record(s)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
@@ -458,12 +474,8 @@ def main():
     time.sleep(0.05)
     clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / K
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = w.entries * world / (ms * 1e-3)
+    ms = max_over_ranks(torch, sum(step_ms) / K, world, dev)
+    value = whole_job_rate(w.entries, world, ms)
     st_timed = stats[base:base + K].cpu().numpy()
 
     # ---- phase split: gather vs commit + copy (separate pass, same stream) ----
@@ -523,10 +535,7 @@ def main():
     e2e_parts = {name: statistics.median(ev[i].elapsed_time(ev[i + 1]) for ev in e2e_ev)
                  for i, name in enumerate(("h2d_ms_median", "swap_in_ms_median",
                                            "d2h_ms_median"))}
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(torch, e2e_ms, world, dev)
     h2d_bytes = n_in * 4
     d2h_bytes = locs_host.numel() * 4
     rc, flags = cache.status()
@@ -555,7 +564,7 @@ def main():
         "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": config_dict(w, world),
-        "e2e": {"value": w.entries * world / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": whole_job_rate(w.entries, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
                 "ms_per_step": e2e_ms, **e2e_parts},
         "gpu_launches": K * n_kernels,
