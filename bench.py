@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--copy-ctas", type=int, default=0)
+    ap.add_argument("--launch", default="graph", choices=["graph", "direct"],
+                    help="timed steps as one replayed CUDA graph per step, or direct launches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--compare-sequential", action="store_true",
@@ -403,7 +405,8 @@ def main():
     K, Wm = args.steps, args.warmup
     n_e2e = min(K, 20)
     n_phase = min(K, 20)
-    total_calls = PREROLL_CALLS + Wm + K + n_phase + n_e2e + 2
+    n_alt = min(K, 20)
+    total_calls = PREROLL_CALLS + Wm + K + n_phase + n_e2e + 2 + n_alt
     stream_gen = W.TopkStream(w)
     calls = stream_gen.calls(total_calls)
     rpi_np, sl_np = W.req_pool_indices(w), W.seq_lens(w)
@@ -443,6 +446,34 @@ def main():
     if flags:
         raise RuntimeError("device status flags %#x after warm-up" % flags)
 
+    # One CUDA graph of a whole step (the way a decode loop replays it): the
+    # step's top-k is staged into the graph's input buffer before its events.
+    topk_buf = torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)
+    stats_buf = torch.empty((Bn, pkg.binding.HS_NUM_STATS), dtype=torch.int32, device=dev)
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        cache.swap_in(rpi, sl, topk_buf, 0, out={"device_locs": locs, "stats": stats_buf},
+                      stream=side)
+        if page_out is not None:
+            cache.page_table(topk_buf, sl, w.page_size, out=page_out, stream=side)
+
+    def run_steps(first, n, mode, events):
+        """n steps from call `first` on, each between its own pair of events."""
+        for k in range(n):
+            i = first + k
+            if mode == "graph":
+                topk_buf.copy_(topk_all[i])
+            flush.fill_(k & 0xFF)
+            events[k][0].record(s)
+            if mode == "graph":
+                graph.replay()
+            else:
+                step(i, topk_all[i])
+            events[k][1].record(s)
+            if mode == "graph":
+                stats[i].copy_(stats_buf)
+
     h2d_peak = measure_h2d_peak(torch, dev)
     peaks = read_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
@@ -461,11 +492,7 @@ def main():
     base = PREROLL_CALLS + Wm
     gate(torch, K)
     torch.cuda.nvtx.range_push("timed_steps")  # lets a profiler select these launches
-    for k in range(K):
-        flush.fill_(k & 0xFF)
-        ev[k][0].record(s)
-        step(base + k, topk_all[base + k])
-        ev[k][1].record(s)
+    run_steps(base, K, args.launch, ev)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -477,6 +504,11 @@ def main():
     ms = max_over_ranks(torch, sum(step_ms) / K, world, dev)
     value = whole_job_rate(w.entries, world, ms)
     st_timed = stats[base:base + K].cpu().numpy()
+    # the other launch mode on the next calls of the stream, for comparison
+    alt = "direct" if args.launch == "graph" else "graph"
+    abase = PREROLL_CALLS + Wm + K + n_phase + n_e2e + 2
+    ev_alt = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n_alt)]
 
     # ---- phase split: gather vs commit + copy (separate pass, same stream) ----
     e_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
@@ -541,6 +573,11 @@ def main():
     rc, flags = cache.status()
     if flags:
         raise RuntimeError("device status flags %#x after the timed region" % flags)
+    torch.cuda.synchronize()
+    gate(torch, n_alt)
+    run_steps(abase, n_alt, alt, ev_alt)
+    torch.cuda.synchronize()
+    alt_ms = sum(a.elapsed_time(b) for a, b in ev_alt) / n_alt
     ceiling = copy_ceiling(torch, pkg, cache, w, dev, flush,
                            float(stats[base:base + K, :, 3].float().mean()))
 
@@ -563,7 +600,10 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": config_dict(w, world),
+        "config": dict(config_dict(w, world), launch=(
+            "one CUDA graph per step (gather + commit/copy), replayed; the step's top-k is "
+            "staged into the graph's input buffer before the step's events"
+            if args.launch == "graph" else "direct launches through the C ABI")),
         "e2e": {"value": whole_job_rate(w.entries, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
                 "ms_per_step": e2e_ms, **e2e_parts},
@@ -583,6 +623,8 @@ def main():
             "unique_misses_per_step": float(np.mean(U_timed)),
             "miss_copy_mb_per_step": float(np.mean(U_timed)) * w.row_bytes / 1e6,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+            "other_launch_mode": {"launch": alt, "ms_per_step": alt_ms, "steps": n_alt,
+                                  "value": whole_job_rate(w.entries, 1, alt_ms)},
         },
         "copy_ceiling": ceiling,
         "clocks": clk,
