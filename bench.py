@@ -38,6 +38,14 @@ if ROOT not in sys.path:
 import hs_workloads as W  # noqa: E402
 
 METRIC = "selected tokens resolved/s per layer-call"
+# Per-launch counters of the current kernels on the C2 workload, from one ncu
+# capture of the timed steps (steady state, after an L2 flush):
+#   commit_copy_kernel: syslts__t_sectors_aperture_sysmem_op_read = 347,942
+#   sectors (host-link reads, 32 B each), dram__bytes_read + write = 8,079,872 B;
+#   gather_kernel: dram__bytes_read + write = 5,837,568 B.
+# Other workloads have no capture, so their traffic is reported as null.
+NCU_TRAFFIC = {"C2": {"commit_copy_host_link_bytes": 347942 * 32,
+                      "commit_copy_dram_bytes": 8079872, "gather_dram_bytes": 5837568}}
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
 FLUSH_BYTES = 256 << 20
@@ -610,7 +618,14 @@ def main():
         "gpu_launches": K * n_kernels,
         "roofline": {"kernel": "commit_copy_kernel (commit CTAs + miss-row copy CTAs)",
                      "bound": "host_link", "achieved": achieved_copy, "peak": h2d_peak,
-                     "unit": "GB/s", "frac": achieved_copy / h2d_peak, "traffic": None,
+                     "unit": "GB/s", "frac": achieved_copy / h2d_peak,
+                     "traffic": NCU_TRAFFIC.get(args.config, {}).get("commit_copy_dram_bytes"),
+                     "host_link_traffic": NCU_TRAFFIC.get(args.config, {}).get(
+                         "commit_copy_host_link_bytes"),
+                     "traffic_note": "traffic = DRAM read+write bytes per launch (the commit's "
+                                     "state rows); host_link_traffic = system-memory read "
+                                     "bytes per launch, the link this kernel is bound by; both "
+                                     "from one ncu capture of this workload",
                      "peak_source": "measured in this run: pinned host->device cudaMemcpyAsync "
                                     "256 MiB, best of 20",
                      "algorithmic_bytes_per_launch": float(np.mean(copy_bytes))},
@@ -618,7 +633,9 @@ def main():
             "gather_ms": float(np.mean(g_ms)), "commit_copy_ms": float(np.mean(cc_ms)),
             "gather_hbm": {"achieved": achieved_gather, "peak": hbm_peak, "unit": "GB/s",
                            "frac": achieved_gather / hbm_peak, "peak_source": hbm_src,
-                           "algorithmic_bytes_per_launch": float(np.mean(gather_bytes))},
+                           "algorithmic_bytes_per_launch": float(np.mean(gather_bytes)),
+                           "traffic": NCU_TRAFFIC.get(args.config, {}).get(
+                               "gather_dram_bytes")},
             "commit_bytes_per_launch": float(np.mean(commit_bytes)),
             "unique_misses_per_step": float(np.mean(U_timed)),
             "miss_copy_mb_per_step": float(np.mean(U_timed)) * w.row_bytes / 1e6,
