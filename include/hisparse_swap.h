@@ -92,7 +92,22 @@ typedef struct hs_config {
     int32_t max_steps;       /* S_max: 1..4 speculative steps                     */
     int32_t num_layers;      /* layers sharing one state object                   */
     int32_t max_batch;       /* B_max: requests per call, <= num_requests         */
+    int32_t index_kind;      /* token -> slot index: HS_INDEX_HASH (0, default) or
+                                HS_INDEX_DENSE (1); see below                       */
 } hs_config;
+
+/* Token -> hot-slot index of each (layer, request).
+ *   HS_INDEX_HASH: an open-addressing hash bank of hash_size int64 entries,
+ *     (t << 32) | slot (the pages' per-request hash banks, PR #32162 report,
+ *     关键源码片段).  Memory per (layer, request): 16 * H bytes or more; a
+ *     lookup probes a short chain; evictions leave deleted entries that a
+ *     rebuild clears.
+ *   HS_INDEX_DENSE: a direct int16 map over the request's positions,
+ *     slot_of[t] (-1 = not resident).  Memory per (layer, request):
+ *     2 * max_seq_len bytes; a lookup is one load, an eviction or admission
+ *     one store.  Results are identical; only speed and memory differ. */
+#define HS_INDEX_HASH 0
+#define HS_INDEX_DENSE 1
 
 typedef struct hs_state hs_state; /* opaque host handle */
 
@@ -108,7 +123,8 @@ int hs_config_check(const hs_config* cfg);
  *   workspace:  device bytes, per-call scratch shared by all layers
  *   device_kv:  device bytes of ONE layer's KV buffer, R * (H + C) * W
  *   host_pool:  pinned host bytes of ONE layer's pool, R * L_max * W
- * `hash_size` is the entries of one request's hash bank (power of two). */
+ * `hash_size` is the entries of one request's hash bank (power of two), or 0
+ * with HS_INDEX_DENSE. */
 size_t hs_state_bytes(const hs_config* cfg);
 size_t hs_workspace_bytes(const hs_config* cfg);
 size_t hs_device_kv_bytes(const hs_config* cfg);
@@ -195,7 +211,8 @@ int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream);
  *   phys_host int32 [H + C]: physical row of each position (a permutation)
  *   ctrl_host int32 [8]: {next epoch, resident count, used hash entries, ...}
  *   bank_host int64 [hash_size]: hash entries (t << 32 | slot), -1 empty,
- *             -2 deleted */
+ *             -2 deleted; with HS_INDEX_DENSE it receives the request's map
+ *             instead, widened: int64 [max_seq_len], slot or -1 */
 int hs_export_request_state(hs_state* st, int32_t layer_id, int32_t request, int32_t* tok_host,
                             int32_t* ep_host, int32_t* phys_host, int32_t* ctrl_host,
                             int64_t* bank_host, void* stream);

@@ -31,6 +31,9 @@ HS_STATUS_SEQ_LEN_CLAMPED = 0x4
 HS_STATUS_PROBE_LIMIT = 0x8
 HS_STATUS_TABLE_FULL = 0x10
 
+HS_INDEX_HASH = 0
+HS_INDEX_DENSE = 1
+
 HS_NUM_STATS = 8
 STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "evicted",
               "overflow", "invalid")
@@ -48,7 +51,8 @@ class HsConfig(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
                 ("item_size_bytes", ctypes.c_int32), ("hot_buffer_size", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("max_steps", ctypes.c_int32),
-                ("num_layers", ctypes.c_int32), ("max_batch", ctypes.c_int32)]
+                ("num_layers", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("index_kind", ctypes.c_int32)]
 
     def as_dict(self) -> Dict[str, int]:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -56,9 +60,11 @@ class HsConfig(ctypes.Structure):
 
 def make_config(num_requests: int, max_seq_len: int, item_size_bytes: int,
                 hot_buffer_size: int, top_k: int, max_steps: int, num_layers: int = 1,
-                max_batch: Optional[int] = None) -> HsConfig:
+                max_batch: Optional[int] = None, index_kind: int = 0) -> HsConfig:
+    """index_kind: HS_INDEX_HASH (0, hash banks) or HS_INDEX_DENSE (1, dense map)."""
     return HsConfig(num_requests, max_seq_len, item_size_bytes, hot_buffer_size, top_k,
-                    max_steps, num_layers, num_requests if max_batch is None else max_batch)
+                    max_steps, num_layers, num_requests if max_batch is None else max_batch,
+                    index_kind)
 
 
 _lib = None
@@ -289,7 +295,9 @@ def hs_export_request_state(handle: StateHandle, layer_id: int, request: int, st
     ep = np.empty(H, np.int32)
     phys = np.empty(H + C, np.int32)
     ctrl = np.empty(8, np.int32)
-    bank = np.empty(hs_hash_size(cfg), np.int64)
+    # hash entries, or the dense map widened to int64 [max_seq_len]
+    bank = np.empty(cfg.max_seq_len if cfg.index_kind == HS_INDEX_DENSE else hs_hash_size(cfg),
+                    np.int64)
     rc = load_library().hs_export_request_state(
         handle.ptr, layer_id, request, tok.ctypes.data, ep.ctypes.data, phys.ctypes.data,
         ctrl.ctypes.data, bank.ctypes.data, _stream_ptr(stream))

@@ -30,8 +30,9 @@ static Dims dims_of(const hs_config& c) {
     d.C = c.max_steps * c.top_k;
     d.layers = c.num_layers;
     d.B_max = c.max_batch;
-    d.hash_size = hash_size_for(c.hot_buffer_size);
-    d.hash_shift = 32 - __builtin_ctz((unsigned)d.hash_size);
+    d.dense = c.index_kind == HS_INDEX_DENSE ? 1 : 0;
+    d.hash_size = d.dense ? 0 : hash_size_for(c.hot_buffer_size);
+    d.hash_shift = d.dense ? 0 : 32 - __builtin_ctz((unsigned)d.hash_size);
     return d;
 }
 
@@ -41,6 +42,8 @@ StateLayout state_layout(const Dims& d) {
     size_t o = 0;
     s.bank = o;
     o = align256(o + lr * d.hash_size * 8);
+    s.map = o;
+    o = align256(o + (d.dense ? lr * d.L * 2 : 0));
     s.ep = o;
     o = align256(o + lr * d.H * 4);
     s.tok = o;
@@ -81,7 +84,8 @@ LayerView layer_view(const Dims& d, uint8_t* state, int layer, const uint8_t* ho
     const size_t lq = (size_t)layer * d.R;
     LayerView v;
     v.bank = reinterpret_cast<long long*>(state + s.bank) + lq * d.hash_size;
-    v.ep = reinterpret_cast<int32_t*>(state + s.ep) + lq * d.H;
+    v.map = reinterpret_cast<int16_t*>(state + s.map) + (d.dense ? lq * d.L : 0);
+    v.ep =reinterpret_cast<int32_t*>(state + s.ep) + lq * d.H;
     v.tok = reinterpret_cast<int32_t*>(state + s.tok) + lq * d.H;
     v.phys = reinterpret_cast<int32_t*>(state + s.phys) + lq * (d.H + d.C);
     v.ctrl = reinterpret_cast<int32_t*>(state + s.ctrl) + lq * kCtrlWords;
@@ -123,6 +127,8 @@ int hs_config_check(const hs_config* c) {
     if (c->max_steps > HS_MAX_STEPS) return HS_ERR_UNSUPPORTED;
     if ((long long)c->max_steps * c->top_k > HS_MAX_ENTRIES) return HS_ERR_UNSUPPORTED;
     if (c->max_batch > 65535 || c->num_layers > 65535) return HS_ERR_UNSUPPORTED;
+    if (c->index_kind != HS_INDEX_HASH && c->index_kind != HS_INDEX_DENSE)
+        return HS_ERR_INVALID_ARG;
     // device rows and host rows must be addressable by int32 indices
     const long long dev_rows =
         (long long)c->num_requests * (c->hot_buffer_size + (long long)c->max_steps * c->top_k);
@@ -373,10 +379,19 @@ int hs_export_request_state(hs_state* st, int32_t layer_id, int32_t request, int
     if (ctrl_host && e == cudaSuccess)
         e = cudaMemcpyAsync(ctrl_host, v.ctrl + q * kCtrlWords, kCtrlWords * 4,
                             cudaMemcpyDeviceToHost, s);
-    if (bank_host && e == cudaSuccess)
-        e = cudaMemcpyAsync(bank_host, v.bank + q * d.hash_size, (size_t)d.hash_size * 8,
-                            cudaMemcpyDeviceToHost, s);
+    std::vector<int16_t> map;
+    if (bank_host && e == cudaSuccess) {
+        if (d.dense) {
+            map.resize((size_t)d.L);
+            e = cudaMemcpyAsync(map.data(), v.map + q * d.L, (size_t)d.L * 2,
+                                cudaMemcpyDeviceToHost, s);
+        } else {
+            e = cudaMemcpyAsync(bank_host, v.bank + q * d.hash_size, (size_t)d.hash_size * 8,
+                                cudaMemcpyDeviceToHost, s);
+        }
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    for (size_t i = 0; i < map.size(); ++i) bank_host[i] = map[i];  // dense map, widened
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;
 }
 

@@ -310,6 +310,15 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
             phys[H + j] = pv;
             tok[v] = t;
             ep[v] = E;
+            if (d.dense) {  // dense index: one store each (old != t: resident vs not)
+                int16_t* map = a.lv.map + (long long)q * d.L;
+                if (old >= 0) {
+                    map[old] = -1;
+                    ++evicted;
+                }
+                map[t] = (int16_t)v;
+                continue;
+            }
             if (old >= 0) {
                 bank_delete(bank, d.hash_shift, hmask, old, a.ws.status);
                 ++evicted;
@@ -324,7 +333,7 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
         }
         __syncthreads();
         // ---- rebuild the bank once deleted entries pile up ---------------------
-        if (s_misc[0] > (d.hash_size / 4) * 3) {
+        if (!d.dense && s_misc[0] > (d.hash_size / 4) * 3) {
             for (int p = tid; p < d.hash_size; p += BD) bank[p] = kEmpty;
             __syncthreads();
             for (int v = tid; v < H; v += BD) {

@@ -112,10 +112,19 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
     {
         long long e[RMAX];
         unsigned pos[RMAX];
+        const int16_t* map = a.lv.map + (long long)(q_ok ? q : 0) * d.L;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             const bool valid = q_ok && (lo + r * BD + tid < hi) && t[r] >= 0 && t[r] < limit;
             code[r] = valid ? kMissPending : -1;
+            if (d.dense) {  // dense index: the slot is one load away, no chain
+                e[r] = kEmpty;
+                if (valid) {
+                    const int slot = map[t[r]];
+                    if (slot >= 0 && slot < d.H) code[r] = slot;
+                }
+                continue;
+            }
             pos[r] = hash_token(t[r], d.hash_shift);
             e[r] = valid ? bank[pos[r]] : kEmpty;
         }

@@ -4,6 +4,8 @@
 //   state (persistent, per layer l and request q):
 //     bank  int64 [layers][R][hash_size]  token -> slot hash, (t << 32) | slot;
 //                                         -1 never used, -2 deleted
+//     map   int16 [layers][R][L]          dense index instead of the bank:
+//                                         slot of each position, -1 absent
 //     ep    int32 [layers][R][H]          epoch of the slot's last reference
 //     tok   int32 [layers][R][H]          token held by the slot (-1 empty)
 //     phys  int32 [layers][R][H + C]      physical row of each position
@@ -45,12 +47,14 @@ enum Cnt : int {
 
 struct Dims {
     int32_t R, L, W, H, K, S_max, C, layers, B_max;
-    int32_t hash_size;   // entries per request bank, power of two (>= 32)
+    int32_t hash_size;   // entries per request bank, power of two (>= 32); 0 if dense
     int32_t hash_shift;  // 32 - log2(hash_size)
+    int32_t dense;       // 1: token -> slot index is the dense map, not the hash bank
 };
 
 struct LayerView {
-    long long* bank;           // [R][hash_size]
+    long long* bank;           // [R][hash_size] (hash index)
+    int16_t* map;              // [R][L] slot of each position, -1 if absent (dense index)
     int32_t* ep;               // [R][H]
     int32_t* tok;              // [R][H]
     int32_t* phys;             // [R][H + C]
@@ -88,7 +92,7 @@ struct SwapArgs {
 
 // Byte offsets of the state and workspace regions (256-byte aligned).
 struct StateLayout {
-    size_t bank, ep, tok, phys, ctrl, total;
+    size_t bank, map, ep, tok, phys, ctrl, total;
 };
 struct WorkspaceLayout {
     size_t miss_tok, miss_last, miss_dst, vict, adm, cnt, status, total;

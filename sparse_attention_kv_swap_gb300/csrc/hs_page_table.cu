@@ -91,6 +91,10 @@ __global__ void reset_kernel(const Dims d, uint8_t* state, StateLayout sl,
     int32_t* phys = reinterpret_cast<int32_t*>(state + sl.phys) + lq * (d.H + d.C);
     int32_t* ctrl = reinterpret_cast<int32_t*>(state + sl.ctrl) + lq * kCtrlWords;
     for (int p = threadIdx.x; p < d.hash_size; p += blockDim.x) bank[p] = kEmpty;
+    if (d.dense) {
+        int16_t* map = reinterpret_cast<int16_t*>(state + sl.map) + lq * d.L;
+        for (int p = threadIdx.x; p < d.L; p += blockDim.x) map[p] = -1;
+    }
     for (int v = threadIdx.x; v < d.H; v += blockDim.x) {
         ep[v] = -1;
         tok[v] = -1;

@@ -12,8 +12,24 @@ from checker import check_call
 from common import row_fn
 
 
-def bank_consistent(st: dict) -> Optional[str]:
+def map_consistent(st: dict) -> Optional[str]:
+    """The dense index maps exactly the resident tokens to their slots."""
+    m = st["bank"]  # the dense map, widened to int64 [max_seq_len]
+    got = {int(t): int(v) for t, v in enumerate(m.tolist()) if v != -1}
+    want = {int(t): v for v, t in enumerate(st["tok"].tolist()) if t != -1}
+    if got != want:
+        return "dense map differs from the slot table"
+    if int((st["tok"] != -1).sum()) != int(st["ctrl"][1]):
+        return "resident counter is wrong"
+    if int(st["ctrl"][3]) != 0:
+        return "request lock still held"
+    return None
+
+
+def bank_consistent(st: dict, dense: bool = False) -> Optional[str]:
     """The hash bank holds exactly the resident (token, slot) pairs."""
+    if dense:
+        return map_consistent(st)
     bank = st["bank"]
     live = bank[bank >= 0]
     pairs = set(zip((live >> 32).astype(np.int64).tolist(),
@@ -34,15 +50,17 @@ def bank_consistent(st: dict) -> Optional[str]:
 
 class ParityRun:
     def __init__(self, R: int, L: int, width: int, H: int, K: int, S_max: int, layers: int = 1,
-                 max_batch: Optional[int] = None, pools=None, deferred: bool = False):
+                 max_batch: Optional[int] = None, pools=None, deferred: bool = False,
+                 dense: bool = False):
         self.deferred = deferred
+        self.dense = dense
         import sparse_attention_kv_swap_gb300 as pkg
         from oracle import Oracle
         from sparse_attention_kv_swap_gb300.cache import SwapInCache
         self.R, self.L, self.W, self.H, self.K, self.S_max = R, L, width, H, K, S_max
         self.C = S_max * K
         self.layers = layers
-        cfg = pkg.make_config(R, L, width, H, K, S_max, layers, max_batch)
+        cfg = pkg.make_config(R, L, width, H, K, S_max, layers, max_batch, index_kind=int(dense))
         if pools is None:
             pools = []
             for l in range(layers):
@@ -105,7 +123,7 @@ class ParityRun:
             for k in ("tok", "ep", "phys"):
                 assert (gs[k] == os_[k]).all(), "%s q=%d: state %s differs" % (tag, q, k)
             assert gs["epoch"] == os_["epoch"], "%s q=%d: epoch differs" % (tag, q)
-            err = bank_consistent(gs)
+            err = bank_consistent(gs, self.dense)
             assert err is None, "%s q=%d: %s" % (tag, q, err)
         dev = self.cache.device_kv[layer]
         if compare_rows:

@@ -124,3 +124,14 @@ def test_page_table_rejects_bad_arguments(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         B.load_library(str(tmp_path / "nope.so"))
+
+
+def test_dense_index_config(lib):
+    hashed, dense = _cfg(), _cfg(index_kind=B.HS_INDEX_DENSE)
+    assert pkg.hs_config_check(dense) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(index_kind=2)) == B.HS_ERR_INVALID_ARG
+    assert pkg.hs_hash_size(dense) == 0
+    # the dense map replaces the 64 x 16384 x 8-byte hash banks by 64 x 32768 x 2 bytes
+    diff = pkg.hs_state_bytes(hashed) - pkg.hs_state_bytes(dense)
+    assert abs(diff - (64 * 16384 * 8 - 64 * 32768 * 2)) <= 512
+    assert pkg.hs_workspace_bytes(dense) == pkg.hs_workspace_bytes(hashed)

@@ -149,3 +149,38 @@ def test_workload_full_size(name):
     for c in range(8):
         run.call(stream.next_call(), rpi, sl, compare_rows=(c % 4 == 3),
                  properties=(name == "C4" and c == 7))
+
+
+# ---- dense token -> slot index (HS_INDEX_DENSE): identical observables --------
+
+@pytest.mark.parametrize("R,L,H,K,S_max,B,calls", SMALL)
+def test_small_configs_dense_index(R, L, H, K, S_max, B, calls):
+    rng = np.random.default_rng(R * 1000 + K)
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max, dense=True)
+    for topk, rpi, sl in _rand_calls(rng, R, L, K, S_max, B, calls):
+        run.call(topk, rpi, sl, properties=True)
+
+
+def test_dense_index_reset_and_layers():
+    import torch
+    rng = np.random.default_rng(12)
+    run = ParityRun(4, 600, W.ROW_BYTES, 50, 32, 2, layers=2, dense=True)
+    calls = list(_rand_calls(rng, 4, 600, 32, 2, 4, 6))
+    for i, (topk, rpi, sl) in enumerate(calls):
+        run.call(topk, rpi, sl, layer=i % 2)
+        if i == 3:
+            victims = np.array([0, 2], np.int32)
+            run.cache.reset_requests(torch.from_numpy(victims).cuda())
+            run.oracle.reset_requests(victims)
+
+
+@pytest.mark.parametrize("name", ["C2", "C3", "C4", "C5"])
+def test_workload_full_size_dense_index(name):
+    w = W.WORKLOADS[name]
+    stream = W.TopkStream(w)
+    rpi = W.req_pool_indices(w)
+    sl = W.seq_lens(w)
+    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, dense=True)
+    for c in range(6):
+        run.call(stream.next_call(), rpi, sl, compare_rows=(c == 5),
+                 properties=(name == "C4" and c == 5))
