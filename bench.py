@@ -59,8 +59,9 @@ def parse_args():
     ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--copy-ctas", type=int, default=0)
-    ap.add_argument("--index", default="hash", choices=["hash", "dense"],
-                    help="token -> slot index: per-request hash banks or a dense map")
+    ap.add_argument("--index", default="dense", choices=["hash", "dense"],
+                    help="token -> slot index: a dense map (faster on GB300 at these "
+                         "sizes) or per-request hash banks")
     ap.add_argument("--launch", default="graph", choices=["graph", "direct"],
                     help="timed steps as one replayed CUDA graph per step, or direct launches")
     ap.add_argument("--no-cpu-baseline", action="store_true")
