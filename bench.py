@@ -39,13 +39,16 @@ import hs_workloads as W  # noqa: E402
 
 METRIC = "selected tokens resolved/s per layer-call"
 # Per-launch counters of the current kernels on the C2 workload, from one ncu
-# capture of the timed steps (steady state, after an L2 flush):
-#   commit_copy_kernel: syslts__t_sectors_aperture_sysmem_op_read = 347,942
-#   sectors (host-link reads, 32 B each), dram__bytes_read + write = 8,079,872 B;
-#   gather_kernel: dram__bytes_read + write = 5,837,568 B.
+# capture of the timed steps (steady state, after an L2 flush), per index:
+#   commit_copy_kernel: syslts__t_sectors_aperture_sysmem_op_read (host-link
+#   reads, 32 B sectors) and dram__bytes_read + write; gather_kernel: DRAM bytes.
 # Other workloads have no capture, so their traffic is reported as null.
-NCU_TRAFFIC = {"C2": {"commit_copy_host_link_bytes": 347942 * 32,
-                      "commit_copy_dram_bytes": 8079872, "gather_dram_bytes": 5837568}}
+NCU_TRAFFIC = {("C2", "dense"): {"commit_copy_host_link_bytes": 347275 * 32,
+                                 "commit_copy_dram_bytes": 3905792 + 25088,
+                                 "gather_dram_bytes": 5005056},
+               ("C2", "hash"): {"commit_copy_host_link_bytes": 347942 * 32,
+                                "commit_copy_dram_bytes": 8077312 + 2560,
+                                "gather_dram_bytes": 5837568}}
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
 FLUSH_BYTES = 256 << 20
@@ -629,8 +632,8 @@ def main():
         "roofline": {"kernel": "commit_copy_kernel (commit CTAs + miss-row copy CTAs)",
                      "bound": "host_link", "achieved": achieved_copy, "peak": h2d_peak,
                      "unit": "GB/s", "frac": achieved_copy / h2d_peak,
-                     "traffic": NCU_TRAFFIC.get(args.config, {}).get("commit_copy_dram_bytes"),
-                     "host_link_traffic": NCU_TRAFFIC.get(args.config, {}).get(
+                     "traffic": NCU_TRAFFIC.get((args.config, args.index), {}).get("commit_copy_dram_bytes"),
+                     "host_link_traffic": NCU_TRAFFIC.get((args.config, args.index), {}).get(
                          "commit_copy_host_link_bytes"),
                      "traffic_note": "traffic = DRAM read+write bytes per launch (the commit's "
                                      "state rows); host_link_traffic = system-memory read "
@@ -644,7 +647,7 @@ def main():
             "gather_hbm": {"achieved": achieved_gather, "peak": hbm_peak, "unit": "GB/s",
                            "frac": achieved_gather / hbm_peak, "peak_source": hbm_src,
                            "algorithmic_bytes_per_launch": float(np.mean(gather_bytes)),
-                           "traffic": NCU_TRAFFIC.get(args.config, {}).get(
+                           "traffic": NCU_TRAFFIC.get((args.config, args.index), {}).get(
                                "gather_dram_bytes")},
             "commit_bytes_per_launch": float(np.mean(commit_bytes)),
             "unique_misses_per_step": float(np.mean(U_timed)),
