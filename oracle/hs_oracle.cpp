@@ -43,6 +43,20 @@
 //     the copied row becomes the hot row without a second copy.
 //  6. Locations are int32 rows of the layer's device buffer:
 //     q * (H + C) + phys[position].
+//  7. Extra page (the gather's first lookup, before the hot-cache hash: the
+//     multi-step swap report, section 实现拆解 item 1).  The page never
+//     defines it; this build reads it as the request's newest, still-filling
+//     page, which stays on the device while decode appends to it.  With
+//     page size E > 0 and n = min(seq_len, L_max), the extra page of a
+//     request holds positions [floor((n - 1) / E) * E, n), position t at
+//     row R * (H + C) + q * E + (t mod E).  A valid entry in that range is
+//     served there: it is neither a hit nor a miss, changes no policy state
+//     and counts only as "extra".  E = 0 turns the page off.
+//  8. Write-back of newly decoded rows (decode keeps idle KV in host memory:
+//     PR #20343 summary, 功能与动机).  Appending row r at (q, t) for a
+//     request of length n writes host row (q, t); the extra-page row of t
+//     if t lies in the extra page of length n; and the hot row of t if t is
+//     resident, so that every copy of (q, t) stays equal.
 #include "hs_oracle.h"
 
 #include <algorithm>
@@ -68,6 +82,7 @@ struct RequestCache {
 
 struct hso_oracle {
     int32_t R, L, W, H, K, S_max, layers, C;
+    int32_t E;  // extra page size, 0 = no extra page
     std::vector<RequestCache> cache;  // [layers * R]
 
     RequestCache& at(int32_t layer, int32_t q) { return cache[(size_t)layer * R + q]; }
@@ -75,6 +90,15 @@ struct hso_oracle {
 };
 
 namespace {
+
+// First position of the extra page of a request whose valid range is
+// [0, n), n >= 1 (reading 7).
+int32_t extra_page_start(int32_t n, int32_t E) { return (n - 1) / E * E; }
+
+// Device row of position t on the extra page of request q (reading 7).
+int64_t extra_row(const hso_oracle& o, int32_t q, int32_t t) {
+    return (int64_t)o.R * (o.H + o.C) + (int64_t)q * o.E + t % o.E;
+}
 
 void make_empty(const hso_oracle& o, RequestCache& rc) {
     rc.res.clear();
@@ -109,6 +133,11 @@ void swap_in_request(const hso_oracle& o, RequestCache& rc, int32_t q, const int
             if (t < 0 || t >= limit) {
                 locs_b[i] = -1;
                 stat[HSO_STAT_INVALID]++;
+                continue;
+            }
+            if (o.E > 0 && t >= extra_page_start(limit, o.E)) {
+                locs_b[i] = (int32_t)extra_row(o, q, t);
+                stat[HSO_STAT_EXTRA]++;
                 continue;
             }
             auto r = rc.res.find(t);
@@ -200,9 +229,9 @@ extern "C" {
 
 hso_oracle* hso_create(int32_t num_requests, int32_t max_seq_len, int32_t item_size_bytes,
                        int32_t hot_buffer_size, int32_t top_k, int32_t max_steps,
-                       int32_t num_layers) {
+                       int32_t num_layers, int32_t extra_page_size) {
     if (num_requests <= 0 || max_seq_len <= 0 || item_size_bytes <= 0 || hot_buffer_size <= 0 ||
-        top_k <= 0 || max_steps <= 0 || num_layers <= 0)
+        top_k <= 0 || max_steps <= 0 || num_layers <= 0 || extra_page_size < 0)
         return nullptr;
     hso_oracle* o = new hso_oracle;
     o->R = num_requests;
@@ -213,6 +242,7 @@ hso_oracle* hso_create(int32_t num_requests, int32_t max_seq_len, int32_t item_s
     o->S_max = max_steps;
     o->layers = num_layers;
     o->C = max_steps * top_k;
+    o->E = extra_page_size;
     o->cache.resize((size_t)num_layers * num_requests);
     for (auto& rc : o->cache) make_empty(*o, rc);
     return o;
@@ -260,6 +290,34 @@ int hso_swap_in(hso_oracle* o, int32_t layer, const uint8_t* host_pool, uint8_t*
         for (auto& th : pool) th.join();
     }
     return HSO_OK;
+}
+
+int hso_append_rows(hso_oracle* o, int32_t layer, uint8_t* host_pool, uint8_t* device_kv,
+                    const int32_t* req, const int32_t* tok, const int32_t* seq_lens,
+                    const uint8_t* rows, int32_t n) {
+    if (!o || layer < 0 || layer >= o->layers || n < 0) return HSO_ERR_ARG;
+    if (n > 0 && (!host_pool || !device_kv || !req || !tok || !seq_lens || !rows))
+        return HSO_ERR_ARG;
+    const int32_t W = o->W;
+    int32_t skipped = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t q = req[i], t = tok[i];
+        const int32_t limit = std::min(seq_lens[i], o->L);
+        if (q < 0 || q >= o->R || t < 0 || t >= limit) {
+            ++skipped;
+            continue;
+        }
+        const uint8_t* row = rows + (int64_t)i * W;
+        std::memcpy(host_pool + ((int64_t)q * o->L + t) * W, row, (size_t)W);
+        if (o->E > 0 && t >= extra_page_start(limit, o->E))
+            std::memcpy(device_kv + extra_row(*o, q, t) * W, row, (size_t)W);
+        const RequestCache& rc = o->at(layer, q);
+        auto r = rc.res.find(t);
+        if (r != rc.res.end())
+            std::memcpy(device_kv + ((int64_t)q * (o->H + o->C) + rc.phys[r->second]) * W, row,
+                        (size_t)W);
+    }
+    return skipped;
 }
 
 int hso_get_request_state(const hso_oracle* o, int32_t layer, int32_t q, int32_t* tok,

@@ -18,9 +18,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hs_oracle.cpp")
 _HDR = os.path.join(_HERE, "hs_oracle.h")
 
-NUM_STATS = 8
+NUM_STATS = 9
 STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "evicted",
-              "overflow", "invalid")
+              "overflow", "invalid", "extra")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,13 +51,16 @@ def build_oracle(src: str = _SRC, out_path: Optional[str] = None, force: bool = 
 
 def _declare(lib) -> None:
     lib.hso_create.restype = ctypes.c_void_p
-    lib.hso_create.argtypes = [ctypes.c_int32] * 7
+    lib.hso_create.argtypes = [ctypes.c_int32] * 8
     lib.hso_destroy.restype = None
     lib.hso_destroy.argtypes = [ctypes.c_void_p]
     lib.hso_swap_in.restype = ctypes.c_int
     lib.hso_swap_in.argtypes = [ctypes.c_void_p, ctypes.c_int32, _u8p, _u8p, _i32p, _i32p, _i32p,
                                 ctypes.c_int32, ctypes.c_int32, _i32p, _i32p, _i64p, _i64p, _i32p,
                                 ctypes.c_int32]
+    lib.hso_append_rows.restype = ctypes.c_int
+    lib.hso_append_rows.argtypes = [ctypes.c_void_p, ctypes.c_int32, _u8p, _u8p, _i32p, _i32p,
+                                    _i32p, _u8p, ctypes.c_int32]
     lib.hso_get_request_state.restype = ctypes.c_int
     lib.hso_get_request_state.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, _i32p,
                                           _i32p, _i32p, _i32p]
@@ -95,13 +98,14 @@ class Oracle:
 
     def __init__(self, num_requests: int, max_seq_len: int, item_size_bytes: int,
                  hot_buffer_size: int, top_k: int, max_steps: int, num_layers: int = 1,
-                 lib=None):
+                 lib=None, extra_page_size: int = 0):
         self.lib = lib if lib is not None else load_library()
         self.R, self.L, self.W = num_requests, max_seq_len, item_size_bytes
         self.H, self.K, self.S_max, self.layers = hot_buffer_size, top_k, max_steps, num_layers
         self.C = max_steps * top_k
+        self.E = extra_page_size
         h = self.lib.hso_create(num_requests, max_seq_len, item_size_bytes, hot_buffer_size,
-                                top_k, max_steps, num_layers)
+                                top_k, max_steps, num_layers, extra_page_size)
         if not h:
             raise ValueError("invalid oracle configuration")
         self._h = ctypes.c_void_p(h)
@@ -144,6 +148,27 @@ class Oracle:
         if want_plan:
             out.update(miss_src=src, miss_dst=dst, miss_count=cnt)
         return out
+
+    def device_rows(self) -> int:
+        """Rows of one layer's device buffer: hot + scratch, then the extra pages."""
+        return self.R * (self.H + self.C + self.E)
+
+    def append_rows(self, layer: int, host_pool: np.ndarray, device_kv: np.ndarray,
+                    req: np.ndarray, tok: np.ndarray, seq_lens: np.ndarray,
+                    rows: np.ndarray) -> int:
+        """Write-back of newly decoded rows; returns the number of skipped entries."""
+        req = np.ascontiguousarray(req, dtype=np.int32)
+        tok = np.ascontiguousarray(tok, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        rows = np.ascontiguousarray(rows, dtype=np.uint8)
+        n = req.size
+        assert tok.size == n and sl.size == n and rows.shape == (n, self.W)
+        rc = self.lib.hso_append_rows(self._h, layer, _ptr(host_pool, _u8p),
+                                      _ptr(device_kv, _u8p), _ptr(req, _i32p), _ptr(tok, _i32p),
+                                      _ptr(sl, _i32p), _ptr(rows, _u8p), n)
+        if rc < 0:
+            raise ValueError("oracle append_rows failed with code %d" % rc)
+        return rc
 
     def request_state(self, layer: int, q: int):
         tok = np.empty(self.H, dtype=np.int32)

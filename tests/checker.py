@@ -24,7 +24,12 @@ multi-step swap report, sections 实现拆解 item 1 and 风险与影响):
       under (last occurrence step descending, first occurrence ascending);
   P4  admitted misses in first-occurrence order occupy ascending slots;
   P5  rotation: an admitted token's hot slot maps to the very row the call
-      returned for it, so locations stay valid after the commit.
+      returned for it, so locations stay valid after the commit;
+and, with an extra page of E rows per request (the newest, still-filling
+page, looked up before the hot cache: same report, 实现拆解 item 1):
+  X1  a valid token in [floor((n - 1) / E) * E, n), n = min(seq_len, L_max),
+      gets row R * (H + C) + q * E + t mod E, and takes no part in hits,
+      misses, admission or the state.
 """
 from __future__ import annotations
 
@@ -33,7 +38,7 @@ from typing import Callable, Dict, List, Optional
 import numpy as np
 
 STAT = {n: i for i, n in enumerate(("hits", "hit_slots", "dup_misses", "unique_misses",
-                                    "admitted", "evicted", "overflow", "invalid"))}
+                                    "admitted", "evicted", "overflow", "invalid", "extra"))}
 
 
 class CheckError(AssertionError):
@@ -67,13 +72,16 @@ def check_call(before: Dict[int, dict], after: Dict[int, dict], topk: np.ndarray
                rpi: np.ndarray, seq_lens: np.ndarray, L_max: int, H: int, C: int,
                locs: np.ndarray, stats: Optional[np.ndarray] = None,
                rows_at: Optional[Callable[[np.ndarray], np.ndarray]] = None,
-               host_row: Optional[Callable[[int, np.ndarray], np.ndarray]] = None) -> None:
+               host_row: Optional[Callable[[int, np.ndarray], np.ndarray]] = None,
+               extra_page: int = 0, R: int = 0) -> None:
     """Check one call.  `before`/`after` map request q -> state dict.
 
     rows_at(locs) returns device rows uint8 [n, W] after the call;
-    host_row(q, tokens) returns the expected host rows uint8 [n, W].
+    host_row(q, tokens) returns the expected host rows uint8 [n, W];
+    extra_page is the extra page size (0: none), R the request-pool size.
     """
     B, S, K = topk.shape
+    Ex = extra_page
     for b in range(B):
         q = int(rpi[b])
         pre, post = before[q], after[q]
@@ -86,6 +94,20 @@ def check_call(before: Dict[int, dict], after: Dict[int, dict], topk: np.ndarray
         valid = (t_flat >= 0) & (t_flat < limit)
         if (l_flat[~valid] != -1).any():
             _fail("%s: invalid entry got a location" % who)
+        # X1: entries on the extra page.
+        extra = np.zeros_like(valid)
+        if Ex > 0 and limit > 0:
+            extra = valid & (t_flat >= (limit - 1) // Ex * Ex)
+            want = R * (H + C) + q * Ex + t_flat[extra] % Ex
+            if (l_flat[extra] != want).any():
+                _fail("%s X1: an extra-page token is not at its extra row" % who)
+        if rows_at is not None and host_row is not None and extra.any():
+            xt = np.unique(t_flat[extra])
+            got = rows_at(R * (H + C) + q * Ex + xt % Ex)
+            if (got != host_row(q, xt)).any():
+                _fail("%s I1: an extra-page row differs from the host row" % who)
+        n_extra = int(extra.sum())
+        valid = valid & ~extra
         res_pre = resident_map(pre["tok"])
         res_post = resident_map(post["tok"])
         vt = t_flat[valid]
@@ -201,7 +223,7 @@ def check_call(before: Dict[int, dict], after: Dict[int, dict], topk: np.ndarray
             evicted = sum(1 for v in vset if pre["tok"][v] != -1)
             exp = {"hits": hits, "hit_slots": len(hit_slots), "dup_misses": n_valid - hits - U,
                    "unique_misses": U, "admitted": m, "evicted": evicted, "overflow": U - m,
-                   "invalid": int((~valid).sum())}
+                   "invalid": int((~valid).sum()) - n_extra, "extra": n_extra}
             for name, val in exp.items():
                 if int(st[STAT[name]]) != val:
                     _fail("%s: stat %s = %d, expected %d" % (who, name, int(st[STAT[name]]), val))

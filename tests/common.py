@@ -22,16 +22,45 @@ def row_fn(layer: int, width: int):
 
 
 class OracleHarness:
-    """Runs calls through the oracle and checks each one with the checker."""
+    """Runs calls through the oracle and checks each one with the checker.
 
-    def __init__(self, R, L, width, H, K, S_max, layers=1, lib=None):
+    Rows appended with `append` are remembered in a plain dict (the latest row
+    of each (layer, q, t)), which the checks use as the expected host row in
+    place of the generator's row."""
+
+    def __init__(self, R, L, width, H, K, S_max, layers=1, lib=None, extra_page=0):
         from oracle import Oracle
-        self.o = Oracle(R, L, width, H, K, S_max, layers, lib=lib)
+        self.o = Oracle(R, L, width, H, K, S_max, layers, lib=lib, extra_page_size=extra_page)
         self.R, self.L, self.W, self.H, self.K, self.S_max = R, L, width, H, K, S_max
         self.C = S_max * K
+        self.E = extra_page
         self.layers = layers
         self.pools = [make_host_pool(R, L, width, l) for l in range(layers)]
-        self.dev = [np.zeros((R * (H + self.C), width), dtype=np.uint8) for _ in range(layers)]
+        self.dev = [np.zeros((R * (H + self.C + extra_page), width), dtype=np.uint8)
+                    for _ in range(layers)]
+        self.latest: Dict[tuple, np.ndarray] = {}
+
+    def host_row(self, layer: int):
+        gen = row_fn(layer, self.W)
+
+        def rows(q: int, toks: np.ndarray) -> np.ndarray:
+            out = gen(q, np.asarray(toks))
+            for i, t in enumerate(np.asarray(toks).tolist()):
+                r = self.latest.get((layer, q, int(t)))
+                if r is not None:
+                    out[i] = r
+            return out
+        return rows
+
+    def append(self, req, tok, seq_lens, rows, layer=0) -> int:
+        """Write-back through the oracle; returns the number of skipped entries."""
+        skipped = self.o.append_rows(layer, self.pools[layer], self.dev[layer], req, tok,
+                                     seq_lens, rows)
+        for q, t, n, r in zip(np.asarray(req).tolist(), np.asarray(tok).tolist(),
+                              np.asarray(seq_lens).tolist(), np.asarray(rows)):
+            if 0 <= q < self.R and 0 <= t < min(n, self.L):
+                self.latest[(layer, q, t)] = np.array(r, dtype=np.uint8)
+        return skipped
 
     def states(self, layer: int) -> Dict[int, dict]:
         return {q: self.o.request_state(layer, q) for q in range(self.R)}
@@ -45,6 +74,7 @@ class OracleHarness:
             dev = self.dev[layer]
             check_call(before, after, np.asarray(topk), np.asarray(rpi), np.asarray(seq_lens),
                        self.L, self.H, self.C, out["locs"], out["stats"],
-                       rows_at=lambda locs: dev[locs], host_row=row_fn(layer, self.W))
+                       rows_at=lambda locs: dev[locs], host_row=self.host_row(layer),
+                       extra_page=self.E, R=self.R)
             out["before"], out["after"] = before, after
         return out

@@ -13,7 +13,18 @@ AssertionError on a mismatch.
   pin_overflow:       overflow cases checked with the property checker;
   pin_782:            the multi-step report's test shape: 782 cross-step
                       unique misses at batch 1 (section 实现拆解 item 4);
-  pin_page_table:     sparse page table equals np.unique of the pages.
+  pin_page_table:     sparse page table equals np.unique of the pages;
+  pin_extra_simulator: with an extra page, random tiny sweeps equal the
+                      brute-force list model (which finds the page by page
+                      index, not by its first position);
+  pin_extra_reduction: an extra-page cache behaves exactly like a cache
+                      without one that is shown the same calls with the
+                      extra-page entries blanked out;
+  pin_append_decode:  a decode loop that appends every new token's row and
+                      rewrites some older ones: every returned row and
+                      every resident row equals the latest row written for
+                      its (request, token) in a plain dict, and so does the
+                      host pool.
 """
 from __future__ import annotations
 
@@ -220,5 +231,104 @@ def pin_page_table(lib) -> None:
             assert (tp[b].reshape(-1) == exp).all()
 
 
+def pin_extra_simulator(lib, trials: int = 30, calls: int = 8) -> None:
+    rng = np.random.default_rng(41)
+    for trial in range(trials):
+        H = int(rng.integers(1, 9))
+        K = int(rng.integers(1, 9))
+        S_max = int(rng.integers(1, 5))
+        R = int(rng.integers(1, 4))
+        E = int(rng.integers(1, 7))
+        L = 16
+        h = OracleHarness(R, L, WIDTH, H, K, S_max, lib=lib, extra_page=E)
+        sims = [ListCache(H, S_max * K, E, R) for _ in range(R)]
+        for c in range(calls):
+            B = int(rng.integers(1, R + 1))
+            S = int(rng.integers(1, S_max + 1))
+            topk, rpi, sl = _random_call(rng, B, R, S, K, L)
+            # lengths that end on, just after and inside a page all occur
+            sl = rng.integers(1, L + 2, size=B).astype(np.int32)
+            out = h.call(topk, rpi, sl, check=False)
+            for b in range(B):
+                q = int(rpi[b])
+                locs, stats = sims[q].call(q, topk[b].tolist(), min(int(sl[b]), L))
+                assert out["locs"][b].tolist() == locs, "extra page: locations differ"
+                assert out["stats"][b].tolist() == stats, "extra page: counters differ"
+                st = h.o.request_state(0, q)
+                assert st["tok"].tolist() == sims[q].tok
+                assert st["ep"].tolist() == sims[q].ep
+                assert st["phys"].tolist() == sims[q].phys
+
+
+def pin_extra_reduction(lib, trials: int = 12, calls: int = 6) -> None:
+    rng = np.random.default_rng(43)
+    for trial in range(trials):
+        H, K, S_max, R = int(rng.integers(2, 12)), int(rng.integers(2, 9)), 3, 3
+        E = int(rng.integers(1, 9))
+        L = 24
+        with_x = OracleHarness(R, L, WIDTH, H, K, S_max, lib=lib, extra_page=E)
+        plain = OracleHarness(R, L, WIDTH, H, K, S_max, lib=lib)
+        for c in range(calls):
+            B = int(rng.integers(1, R + 1))
+            S = int(rng.integers(1, S_max + 1))
+            topk, rpi, sl = _random_call(rng, B, R, S, K, L)
+            a = with_x.call(topk, rpi, sl, check=False)
+            blank = topk.copy()
+            for b in range(B):
+                n = min(int(sl[b]), L)
+                on_page = (topk[b] >= 0) & (topk[b] < n) & (topk[b] // E == (n - 1) // E)
+                blank[b][on_page] = -1
+            p = plain.call(blank, rpi, sl, check=False)
+            kept = blank >= 0
+            assert (a["locs"][kept] == p["locs"][kept]).all(), "non-extra locations differ"
+            sa, sp = a["stats"], p["stats"]
+            assert (sa[:, :7] == sp[:, :7]).all(), "policy counters differ"
+            assert (sa[:, 7] + sa[:, 8] == sp[:, 7]).all(), "extra + invalid != blanked"
+            for q in range(R):
+                x, y = with_x.o.request_state(0, q), plain.o.request_state(0, q)
+                for k in ("tok", "ep", "phys"):
+                    assert (x[k] == y[k]).all(), "state %s differs" % k
+
+
+def pin_append_decode(lib, trials: int = 6, steps: int = 24) -> None:
+    rng = np.random.default_rng(47)
+    for trial in range(trials):
+        R, H, K, S_max = 3, int(rng.integers(2, 10)), int(rng.integers(2, 7)), 2
+        E = int(rng.integers(1, 6))
+        L = 64
+        h = OracleHarness(R, L, WIDTH, H, K, S_max, lib=lib, extra_page=E)
+        n = rng.integers(4, 20, size=R).astype(np.int32)
+        # prefill: the still-filling page of each request is written once
+        for q in range(R):
+            toks = np.arange((n[q] - 1) // E * E, n[q], dtype=np.int32)
+            rows = rng.integers(0, 256, size=(toks.size, WIDTH), dtype=np.uint8)
+            assert h.append(np.full(toks.size, q, np.int32), toks, np.full(toks.size, n[q]),
+                            rows) == 0
+        for step in range(steps):
+            # decode appends one token per request, plus a rewrite of an older one
+            n = np.minimum(n + 1, L).astype(np.int32)
+            req = np.arange(R, dtype=np.int32)
+            tok = n - 1
+            old = rng.integers(0, n).astype(np.int32)
+            req2 = np.concatenate([req, req])
+            tok2 = np.concatenate([tok, old])
+            keep = np.ones(2 * R, bool)
+            keep[R:] = old != tok  # one row per (request, token) per call
+            rows = rng.integers(0, 256, size=(2 * R, WIDTH), dtype=np.uint8)
+            assert h.append(req2[keep], tok2[keep], np.concatenate([n, n])[keep],
+                            rows[keep]) == 0
+            # an out-of-range entry is skipped
+            assert h.append(np.array([0], np.int32), np.array([n[0]], np.int32),
+                            np.array([n[0]], np.int32), rows[:1]) == 1
+            S = int(rng.integers(1, S_max + 1))
+            recent = (n[:, None, None] - 1 - rng.integers(0, 3 * E + 2, size=(R, S, K)))
+            spread = rng.integers(0, n[:, None, None], size=(R, S, K))
+            topk = np.where(rng.random((R, S, K)) < 0.5, recent, spread).astype(np.int32)
+            h.call(topk, req, n)
+        for (layer, q, t), r in h.latest.items():
+            assert (h.pools[layer][q, t] == r).all(), "host pool row not written back"
+
+
 ALL_PINS = (pin_lru, pin_first_call, pin_repeat_call, pin_invariants, pin_simulator,
-            pin_overflow, pin_782, pin_page_table)
+            pin_overflow, pin_782, pin_page_table, pin_extra_simulator, pin_extra_reduction,
+            pin_append_decode)

@@ -6,6 +6,10 @@ and repeated arg-min / arg-max selection instead of sorting.  It tracks only
 the observable policy state per request (slot -> token, slot -> epoch,
 position -> physical row, next epoch) and returns locations and counters.
 Used only on tiny inputs, where its quadratic loops are cheap.
+
+With an extra page of E rows (E > 0), a valid token on the same page as the
+request's newest position (t // E == (limit - 1) // E) is served from row
+R * (H + C) + q * E + t % E and touches nothing else.
 """
 from __future__ import annotations
 
@@ -13,8 +17,8 @@ from typing import List
 
 
 class ListCache:
-    def __init__(self, H: int, C: int):
-        self.H, self.C = H, C
+    def __init__(self, H: int, C: int, E: int = 0, R: int = 0):
+        self.H, self.C, self.E, self.R = H, C, E, R
         self.tok: List[int] = [-1] * H
         self.ep: List[int] = [-1] * H
         self.phys: List[int] = list(range(H + C))
@@ -35,13 +39,17 @@ class ListCache:
         last: List[int] = []  # last step of each miss
         hit_slots: List[int] = []
         locs = []
-        hits = dups = invalid = 0
+        hits = dups = invalid = extra = 0
         for s, row in enumerate(tokens_by_step):
             out = []
             for t in row:
                 if t < 0 or t >= limit:
                     out.append(-1)
                     invalid += 1
+                    continue
+                if self.E and t // self.E == (limit - 1) // self.E:
+                    out.append(self.R * (H + C) + q * self.E + t % self.E)
+                    extra += 1
                     continue
                 v = self.slot_of(t)
                 if v >= 0:
@@ -94,5 +102,5 @@ class ListCache:
             self.tok[v] = misses[j]
             self.ep[v] = E
         self.epoch = E + 1
-        stats = [hits, len(hit_slots), dups, U, m, evicted, U - m, invalid]
+        stats = [hits, len(hit_slots), dups, U, m, evicted, U - m, invalid, extra]
         return locs, stats

@@ -39,6 +39,18 @@ MUTANTS = {
     "seq_len_ignored": ("const int32_t limit = std::min(seq_len, o.L);",
                         "const int32_t limit = o.L;"),
     "evictions_not_counted": ("stat[HSO_STAT_EVICTED]++;", ""),
+    "extra_page_ignored": ("if (o.E > 0 && t >= extra_page_start(limit, o.E)) {",
+                           "if (false) {"),
+    "extra_page_starts_at_length": ("return (n - 1) / E * E;", "return n / E * E;"),
+    "extra_row_ignores_request": ("(int64_t)q * o.E + t % o.E;", "t % o.E;"),
+    "append_skips_extra_row": ("std::memcpy(device_kv + extra_row(*o, q, t) * W, row, (size_t)W);",
+                               ";"),
+    "append_skips_hot_copy": ("if (r != rc.res.end())\n            std::memcpy(",
+                              "if (false)\n            std::memcpy("),
+    "append_ignores_page": ("if (o->E > 0 && t >= extra_page_start(limit, o->E))",
+                            "if (o->E > 0)"),
+    "append_skips_host": ("std::memcpy(host_pool + ((int64_t)q * o->L + t) * W, row, (size_t)W);",
+                          ";"),
 }
 
 
