@@ -301,6 +301,73 @@ def copy_ceiling(torch, pkg, cache, w, dev, flush, rows_per_request, reps=10):
     return out
 
 
+def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256, n=20):
+    """Decode step with the extra page on: per step, the write-back of one new
+    row per request (hs_append_rows: host pool over the host link, extra page
+    and hot copy in HBM), then the swap-in with the newest E positions of
+    every request served from its extra page.  A fresh cache on the same host
+    pool, pre-rolled like the main measurement; the extra page is filled once
+    (prefill) before."""
+    from sparse_attention_kv_swap_gb300.cache import SwapInCache
+    Bn, L, Wr = w.batch, w.seq_len, w.row_bytes
+    cfg = pkg.make_config(Bn, L, Wr, w.hot_buffer, w.top_k, w.steps, 1,
+                          index_kind=1 if dense else 0, extra_page_size=E)
+    cache = SwapInCache(cfg, host_pools=[pool], device=dev)
+    rpi = torch.from_numpy(W.req_pool_indices(w)).to(dev)
+    sl = torch.from_numpy(W.seq_lens(w)).to(dev)
+    q = torch.arange(Bn, dtype=torch.int32, device=dev)
+    page = torch.arange((L - 1) // E * E, L, dtype=torch.int32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    pre_rows = torch.randint(0, 256, (Bn * page.numel(), Wr), dtype=torch.uint8, device=dev,
+                             generator=gen)
+    cache.append_rows(q.repeat_interleave(page.numel()), page.repeat(Bn),
+                      torch.full((Bn * page.numel(),), L, dtype=torch.int32, device=dev),
+                      pre_rows)
+    new_tok = torch.full((Bn,), L - 1, dtype=torch.int32, device=dev)
+    new_len = torch.full((Bn,), L, dtype=torch.int32, device=dev)
+    rows = torch.randint(0, 256, (n + PREROLL_CALLS, Bn, Wr), dtype=torch.uint8, device=dev,
+                         generator=gen)
+    topk_all = torch.from_numpy(np.stack(calls[:PREROLL_CALLS + n])).to(dev)
+    locs = torch.empty((Bn, w.steps, w.top_k), dtype=torch.int32, device=dev)
+    stats = torch.zeros((PREROLL_CALLS + n, Bn, pkg.binding.HS_NUM_STATS), dtype=torch.int32,
+                        device=dev)
+    s = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(PREROLL_CALLS + n):
+        k = i - PREROLL_CALLS
+        if k == 0:
+            torch.cuda.synchronize()
+            gate(torch, n)
+        flush.fill_(i & 0xFF)
+        if k >= 0:
+            ev[k][0].record(s)
+        cache.append_rows(q, new_tok, new_len, rows[i])
+        if k >= 0:
+            ev[k][1].record(s)
+        cache.swap_in(rpi, sl, topk_all[i], 0, out={"device_locs": locs, "stats": stats[i]})
+        if k >= 0:
+            ev[k][2].record(s)
+    torch.cuda.synchronize()
+    rc, flags = cache.status()
+    if flags:
+        raise RuntimeError("device status flags %#x in the decode-step measurement" % flags)
+    app = [e[0].elapsed_time(e[1]) for e in ev]
+    swp = [e[1].elapsed_time(e[2]) for e in ev]
+    pair = [e[0].elapsed_time(e[2]) for e in ev]
+    st = stats[PREROLL_CALLS:].cpu().numpy()
+    ms = statistics.mean(pair)
+    cache.close()
+    return {"extra_page_size": E, "steps": n, "launch": "direct launches through the C ABI",
+            "ms_per_step": ms, "value": w.entries / (ms * 1e-3), "unit": UNIT,
+            "append_ms_median": statistics.median(app),
+            "swap_in_ms_median": statistics.median(swp),
+            "append_rows_per_step": Bn, "append_bytes_per_step": Bn * Wr,
+            "extra_entries_fraction": float(st[:, :, 8].sum() / (n * w.entries)),
+            "unique_misses_per_step": float(st[:, :, 3].sum(axis=1).mean()),
+            "gpu_launches_per_step": 3}
+
+
 def run_compare_sequential(args, w):
     """Multi-step swap (one S-step call) against sequential per-step swap (S
     single-step calls) on the same index stream, each captured as a CUDA
@@ -601,6 +668,8 @@ def main():
     alt_ms = sum(a.elapsed_time(b) for a, b in ev_alt) / n_alt
     ceiling = copy_ceiling(torch, pkg, cache, w, dev, flush,
                            float(stats[base:base + K, :, 3].float().mean()))
+    decode = decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool,
+                                    args.index == "dense", n=min(K, 20))
 
     # ---- roofline bookkeeping (algorithmic bytes) ----
     U_phase = st_phase[:, :, 3].sum(axis=1).astype(np.float64)
@@ -658,6 +727,7 @@ def main():
                                   "value": whole_job_rate(w.entries, 1, alt_ms)},
         },
         "copy_ceiling": ceiling,
+        "decode_step_extra_page": decode,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

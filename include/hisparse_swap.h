@@ -36,10 +36,14 @@
  *    max_seq_len); invalid entries get location -1 and change nothing.
  *  - Layouts (row-major, densest index last):
  *      host pool of layer l      uint8 [R, max_seq_len, W], row (q, t)
- *      device KV buffer of layer uint8 [R, H + C, W], C = max_steps * top_k
+ *      device KV buffer of layer uint8 [R * (H + C) + R * E, W] with
+ *                                C = max_steps * top_k, E = extra_page_size:
+ *                                first request q's H hot + C scratch rows at
+ *                                q * (H + C) + p, then request q's extra page
+ *                                at R * (H + C) + q * E + (t mod E)
  *      top-k indices             int32 [B, S, top_k]
  *      device_locs               int32 [B, S, top_k]: row index into the
- *                                layer's device KV buffer (q * (H + C) + p)
+ *                                layer's device KV buffer
  */
 #ifndef HISPARSE_SWAP_H
 #define HISPARSE_SWAP_H
@@ -65,6 +69,7 @@ extern "C" {
 #define HS_STATUS_SEQ_LEN_CLAMPED 0x4u   /* seq_lens[b] > max_seq_len          */
 #define HS_STATUS_PROBE_LIMIT 0x8u       /* hash probe exceeded the table      */
 #define HS_STATUS_TABLE_FULL 0x10u       /* hash insert found no free entry    */
+#define HS_STATUS_BAD_APPEND 0x20u       /* hs_append_rows entry out of range  */
 
 /* ---- per-request counters of one call (int32 [B, HS_NUM_STATS]) -------- */
 #define HS_STAT_HITS 0          /* valid entries whose token was resident   */
@@ -75,13 +80,15 @@ extern "C" {
 #define HS_STAT_EVICTED 5       /* admitted into a slot that held a token   */
 #define HS_STAT_OVERFLOW 6      /* U - m: served this call, not admitted    */
 #define HS_STAT_INVALID 7       /* entries outside [0, min(seq_len, L_max)) */
-#define HS_NUM_STATS 8
+#define HS_STAT_EXTRA 8         /* valid entries served by the extra page   */
+#define HS_NUM_STATS 9
 
 /* Limits of this build. */
 #define HS_MAX_HOT_BUFFER 32768  /* hot_buffer_size upper bound (PR #32162 report, 风险与影响) */
 #define HS_MAX_STEPS 4           /* speculative steps per call (same report, 实现拆解 item 2) */
 #define HS_MAX_ENTRIES 8192      /* max_steps * top_k per request per call */
 #define HS_MAX_PAGES 262144      /* ceil(max_seq_len / page_size) for hs_page_table */
+#define HS_MAX_EXTRA_PAGE 65536  /* extra_page_size upper bound */
 
 typedef struct hs_config {
     int32_t num_requests;    /* R: request-pool slots (req_pool_indices range)    */
@@ -94,7 +101,21 @@ typedef struct hs_config {
     int32_t max_batch;       /* B_max: requests per call, <= num_requests         */
     int32_t index_kind;      /* token -> slot index: HS_INDEX_HASH (0, default) or
                                 HS_INDEX_DENSE (1); see below                       */
+    int32_t extra_page_size; /* E: rows of each request's extra page, 0 = none;
+                                see below                                          */
 } hs_config;
+
+/* Extra page (the gather's first lookup, ahead of the hot-cache hash: "[HiSparse]
+ * Support hisparse multi-step swap io kernel", 实现拆解 item 1; the page does not
+ * define it, and this library reads it as the request's newest, still-filling
+ * page).  With E > 0 every request q owns E device rows, and for a call with
+ * n = min(seq_len, max_seq_len) the positions [floor((n - 1) / E) * E, n) are
+ * the extra page: a selected token t there gets location
+ * R * (H + C) + q * E + (t mod E) without a lookup, is neither a hit nor a
+ * miss, changes no policy state and counts as HS_STAT_EXTRA.  The caller
+ * fills those rows with hs_append_rows as decode produces them (and once for
+ * the partial last page after prefill); the library never copies them from
+ * the host pool. */
 
 /* Token -> hot-slot index of each (layer, request).
  *   HS_INDEX_HASH: an open-addressing hash bank of hash_size int64 entries,
@@ -121,7 +142,7 @@ int hs_config_check(const hs_config* cfg);
  *               (hash banks, slot epochs, slot tokens, position table,
  *               control words)
  *   workspace:  device bytes, per-call scratch shared by all layers
- *   device_kv:  device bytes of ONE layer's KV buffer, R * (H + C) * W
+ *   device_kv:  device bytes of ONE layer's KV buffer, R * (H + C + E) * W
  *   host_pool:  pinned host bytes of ONE layer's pool, R * L_max * W
  * `hash_size` is the entries of one request's hash bank (power of two), or 0
  * with HS_INDEX_DENSE. */
@@ -169,7 +190,8 @@ void hs_destroy_state(hs_state* st);
  *   miss_count_dev       int32 [batch] out or NULL: unique misses U
  *   (the three miss-plan pointers are all NULL or all non-NULL; entries
  *    j >= U are left untouched)
- * Locations stay valid until the next call on the same layer.  Launches two
+ * Locations stay valid until the next call on the same layer (extra-page
+ * locations: until hs_append_rows rewrites that row).  Launches two
  * kernels on `stream`; the second uses programmatic dependent launch. */
 int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t* seq_lens_dev,
                const int32_t* topk_dev, int32_t batch, int32_t num_steps, int32_t layer_id,
@@ -192,6 +214,29 @@ int hs_page_table(const int32_t* topk_dev, const int32_t* seq_lens_dev, int32_t 
                   int32_t num_steps, int32_t top_k, int32_t max_seq_len, int32_t page_size,
                   int32_t* pages_dev, int32_t* num_pages_dev, int32_t* token_page_dev,
                   void* stream);
+
+/* Write-back of newly decoded KV rows of layer `layer_id` (decode keeps idle
+ * KV in host memory: PR #20343 summary, 功能与动机).
+ *   req_dev      int32 [n]: request slot q of entry i
+ *   tok_dev      int32 [n]: position t of entry i
+ *   seq_lens_dev int32 [n]: the request's length once entry i is in (t < it)
+ *   rows_dev     uint8 [n, W], 16-byte aligned, device memory: the KV rows
+ * For every entry with 0 <= q < R and 0 <= t < min(seq_len, max_seq_len):
+ *   - host pool row (q, t) := the row (written through the pool's device
+ *     mapping; the caller's pool memory is modified);
+ *   - if E > 0 and t lies on the extra page of length seq_len: extra-page
+ *     row R * (H + C) + q * E + (t mod E) := the row;
+ *   - if t is resident in a hot slot of (layer_id, q): that slot's device
+ *     row := the row.
+ * So every copy of (q, t) stays equal.  Other entries are skipped and set
+ * HS_STATUS_BAD_APPEND.  The (q, t) pairs of one call must be distinct
+ * (with duplicates the rows written are unspecified).  Order it on the same
+ * stream as the swap-ins of the layer: before the swap-in whose selection
+ * may include the appended tokens.  Asynchronous on `stream`; n = 0 is a
+ * no-op. */
+int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
+                   const int32_t* tok_dev, const int32_t* seq_lens_dev, const void* rows_dev,
+                   int32_t n, void* stream);
 
 /* Returns requests to the empty state in every layer (use when a request
  * slot is given to a new sequence; order it after the previous user's last

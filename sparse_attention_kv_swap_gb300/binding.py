@@ -30,13 +30,15 @@ HS_STATUS_DUPLICATE_REQUEST = 0x2
 HS_STATUS_SEQ_LEN_CLAMPED = 0x4
 HS_STATUS_PROBE_LIMIT = 0x8
 HS_STATUS_TABLE_FULL = 0x10
+HS_STATUS_BAD_APPEND = 0x20
 
 HS_INDEX_HASH = 0
 HS_INDEX_DENSE = 1
 
-HS_NUM_STATS = 8
+HS_NUM_STATS = 9
 STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "evicted",
-              "overflow", "invalid")
+              "overflow", "invalid", "extra")
+HS_MAX_EXTRA_PAGE = 65536
 
 HEADER = os.path.join(_build.INCLUDE, "hisparse_swap.h")
 
@@ -52,7 +54,7 @@ class HsConfig(ctypes.Structure):
                 ("item_size_bytes", ctypes.c_int32), ("hot_buffer_size", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("max_steps", ctypes.c_int32),
                 ("num_layers", ctypes.c_int32), ("max_batch", ctypes.c_int32),
-                ("index_kind", ctypes.c_int32)]
+                ("index_kind", ctypes.c_int32), ("extra_page_size", ctypes.c_int32)]
 
     def as_dict(self) -> Dict[str, int]:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -60,11 +62,13 @@ class HsConfig(ctypes.Structure):
 
 def make_config(num_requests: int, max_seq_len: int, item_size_bytes: int,
                 hot_buffer_size: int, top_k: int, max_steps: int, num_layers: int = 1,
-                max_batch: Optional[int] = None, index_kind: int = 0) -> HsConfig:
-    """index_kind: HS_INDEX_HASH (0, hash banks) or HS_INDEX_DENSE (1, dense map)."""
+                max_batch: Optional[int] = None, index_kind: int = 0,
+                extra_page_size: int = 0) -> HsConfig:
+    """index_kind: HS_INDEX_HASH (0, hash banks) or HS_INDEX_DENSE (1, dense map);
+    extra_page_size: rows of each request's extra page (0 = none)."""
     return HsConfig(num_requests, max_seq_len, item_size_bytes, hot_buffer_size, top_k,
                     max_steps, num_layers, num_requests if max_batch is None else max_batch,
-                    index_kind)
+                    index_kind, extra_page_size)
 
 
 _lib = None
@@ -95,6 +99,7 @@ def _declare(lib) -> None:
                                                    _vp]),
         "hs_swap_in_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
                                               _vp, _vp, _vp, _vp]),
+        "hs_append_rows": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
         "hs_set_phase_event": (ctypes.c_int, [_vp, _vp]),
         "hs_set_defer_copy": (ctypes.c_int, [_vp, _i32]),
         "hs_copy_planned": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
@@ -304,6 +309,21 @@ def hs_export_request_state(handle: StateHandle, layer_id: int, request: int, st
     _check(rc, "hs_export_request_state")
     return {"tok": tok, "ep": ep, "phys": phys, "ctrl": ctrl, "bank": bank,
             "epoch": int(ctrl[0])}
+
+
+def hs_append_rows(handle: StateHandle, layer_id: int, req, tok, seq_lens, rows,
+                   stream=None) -> None:
+    """Write-back of newly decoded rows: req/tok/seq_lens int32 [n], rows uint8
+    [n, W] on the device (see the C header)."""
+    import torch
+    n = req.numel()
+    if tok.numel() != n or seq_lens.numel() != n or rows.dim() != 2 or rows.shape[0] != n:
+        raise ValueError("req, tok, seq_lens and rows must describe the same n entries")
+    rc = load_library().hs_append_rows(
+        handle.ptr, layer_id, _dptr(req, torch.int32, "req"), _dptr(tok, torch.int32, "tok"),
+        _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(rows, torch.uint8, "rows"), n,
+        _stream_ptr(stream))
+    _check(rc, "hs_append_rows")
 
 
 def hs_set_phase_event(handle: StateHandle, event=None) -> None:

@@ -26,8 +26,10 @@ class SwapInCache:
             host_pools = [torch.empty((R, L, W), dtype=torch.uint8, pin_memory=True)
                           for _ in range(cfg.num_layers)]
         self.host_pools = host_pools
-        self.device_kv = [torch.empty((R * (self.H + self.C), W), dtype=torch.uint8,
-                                      device=self.device) for _ in range(cfg.num_layers)]
+        self.E = cfg.extra_page_size
+        rows = B.hs_device_kv_bytes(cfg) // W  # hot + scratch rows, then the extra pages
+        self.device_kv = [torch.empty((rows, W), dtype=torch.uint8, device=self.device)
+                          for _ in range(cfg.num_layers)]
         self.state = torch.empty(B.hs_state_bytes(cfg), dtype=torch.uint8, device=self.device)
         self.workspace = torch.empty(B.hs_workspace_bytes(cfg), dtype=torch.uint8,
                                      device=self.device)
@@ -62,6 +64,11 @@ class SwapInCache:
         B.hs_page_table(topk, seq_lens, self.cfg.max_seq_len, page_size, o["pages"],
                         o["num_pages"], o["token_page"], stream)
         return o
+
+    def append_rows(self, req: torch.Tensor, tok: torch.Tensor, seq_lens: torch.Tensor,
+                    rows: torch.Tensor, layer_id: int = 0, stream=None) -> None:
+        """Write-back of newly decoded KV rows (host pool, extra page, hot copy)."""
+        B.hs_append_rows(self.handle, layer_id, req, tok, seq_lens, rows, stream)
 
     def reset_requests(self, req_pool_indices: torch.Tensor, stream=None) -> None:
         B.hs_reset_requests(self.handle, req_pool_indices, stream)

@@ -33,6 +33,7 @@ static Dims dims_of(const hs_config& c) {
     d.dense = c.index_kind == HS_INDEX_DENSE ? 1 : 0;
     d.hash_size = d.dense ? 0 : hash_size_for(c.hot_buffer_size);
     d.hash_shift = d.dense ? 0 : 32 - __builtin_ctz((unsigned)d.hash_size);
+    d.E = c.extra_page_size;
     return d;
 }
 
@@ -129,9 +130,12 @@ int hs_config_check(const hs_config* c) {
     if (c->max_batch > 65535 || c->num_layers > 65535) return HS_ERR_UNSUPPORTED;
     if (c->index_kind != HS_INDEX_HASH && c->index_kind != HS_INDEX_DENSE)
         return HS_ERR_INVALID_ARG;
+    if (c->extra_page_size < 0) return HS_ERR_INVALID_ARG;
+    if (c->extra_page_size > HS_MAX_EXTRA_PAGE) return HS_ERR_UNSUPPORTED;
     // device rows and host rows must be addressable by int32 indices
     const long long dev_rows =
-        (long long)c->num_requests * (c->hot_buffer_size + (long long)c->max_steps * c->top_k);
+        (long long)c->num_requests * (c->hot_buffer_size + (long long)c->max_steps * c->top_k +
+                                      c->extra_page_size);
     if (dev_rows > 0x7fffffffLL) return HS_ERR_UNSUPPORTED;
     if ((long long)c->num_requests * c->max_seq_len > 0x7fffffffffffLL) return HS_ERR_UNSUPPORTED;
     return HS_OK;
@@ -150,7 +154,7 @@ size_t hs_workspace_bytes(const hs_config* c) {
 size_t hs_device_kv_bytes(const hs_config* c) {
     if (hs_config_check(c) != HS_OK) return 0;
     const Dims d = dims_of(*c);
-    return (size_t)d.R * (d.H + d.C) * d.W;
+    return (size_t)d.R * (d.H + d.C + d.E) * d.W;
 }
 
 size_t hs_host_pool_bytes(const hs_config* c) {
@@ -276,6 +280,28 @@ int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t*
     if (launch_commit_copy(a, copy_ctas, st->phase_event == nullptr, s) != cudaSuccess)
         return HS_ERR_CUDA;
     return HS_OK;
+}
+
+int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
+                   const int32_t* tok_dev, const int32_t* seq_lens_dev, const void* rows_dev,
+                   int32_t n, void* stream) {
+    if (!st) return HS_ERR_INVALID_ARG;
+    const Dims& d = st->d;
+    if (layer_id < 0 || layer_id >= d.layers || n < 0) return HS_ERR_INVALID_ARG;
+    if (n == 0) return HS_OK;
+    if (!req_dev || !tok_dev || !seq_lens_dev || !rows_dev || !aligned(rows_dev, 16))
+        return HS_ERR_INVALID_ARG;
+    const LayerView lv = layer_view(d, st->state, layer_id, st->host_pool_dev[layer_id],
+                                    st->device_kv[layer_id]);
+    // The pool is the caller's writable memory; the view holds it as const
+    // because the swap-in only reads it.
+    uint8_t* pool = const_cast<uint8_t*>(st->host_pool_dev[layer_id]);
+    const Workspace ws = workspace_view(d, st->ws);
+    return launch_append(d, lv, pool, req_dev, tok_dev, seq_lens_dev,
+                         static_cast<const uint8_t*>(rows_dev), n, ws.status,
+                         static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HS_OK
+               : HS_ERR_CUDA;
 }
 
 int hs_set_defer_copy(hs_state* st, int32_t defer) {
@@ -407,6 +433,6 @@ const char* hs_status_string(int code) {
     }
 }
 
-int32_t hs_version(void) { return 100; }
+int32_t hs_version(void) { return 10100; }
 
 }  // extern "C"

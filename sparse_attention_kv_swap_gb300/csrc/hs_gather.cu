@@ -7,8 +7,11 @@
 // looks tokens up in the hot cache's token -> slot hash and de-duplicates
 // misses across steps).  CTA rank c owns the c-th contiguous slice of the
 // flattened entries.  P is chosen so that B * P CTAs about fill the GPU.
-//   1. each thread loads up to RMAX entries and probes the request's hash
-//      bank (linear probing, all first probes issued before any resolves);
+//   1. each thread loads up to RMAX entries; an entry on the request's extra
+//      page (its newest, still-filling page, the first lookup the same report
+//      lists) is served from its extra row and skips everything below; the
+//      others probe the request's token -> slot index (hash bank: linear
+//      probing, all first probes issued before any resolves; or dense map);
 //   2. misses are de-duplicated in a table distributed over the cluster's
 //      shared memory: a token's home CTA and start position come from its
 //      hash, its probe chain stays in the home CTA, and remote atomics keep
@@ -17,7 +20,8 @@
 //   3. first occurrences are numbered j = 0, 1, ... in (step, k) order: a
 //      block scan inside each CTA plus the totals of lower-ranked CTAs;
 //   4. every entry gets its device row: q * (H + C) + phys[slot] for a hit,
-//      q * (H + C) + phys[H + j] for miss j.  Hit slots take the call's epoch;
+//      q * (H + C) + phys[H + j] for miss j, R * (H + C) + q * E + t mod E
+//      on the extra page.  Hit slots take the call's epoch;
 //      unique misses are listed for the commit (token, last step) and the
 //      copy (destination row).
 // The row copy itself runs in the second kernel, spread over the whole GPU.
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
     int* first = keys + TS;                                     // first index, later ordinal
     unsigned* smask = reinterpret_cast<unsigned*>(first + TS);  // 8 step bits per position
     int* wcount = reinterpret_cast<int*>(smask + (TS >> 2));    // [RMAX][32] warp counts
-    __shared__ int s_ok, s_epoch, s_total, s_cnt[3];
+    __shared__ int s_ok, s_epoch, s_total, s_cnt[4];
 
     const Dims& d = a.d;
     const int b = blockIdx.x / P;
@@ -92,6 +96,9 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
     }
     const bool q_ok = q >= 0 && q < d.R;
     const int limit = sl < d.L ? sl : d.L;
+    // first position of the extra page (past every valid token if none)
+    const int xstart = (d.E > 0 && limit > 0) ? (limit - 1) / d.E * d.E : 0x7fffffff;
+    unsigned xbits = 0u;  // bit r: entry r is on the extra page
     const long long base = (long long)q * (d.H + d.C);
     const int32_t* phys = a.lv.phys + base;
     for (int i = tid; i < TS; i += BD) {
@@ -99,7 +106,7 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
         first[i] = 0x7fffffff;
     }
     for (int i = tid; i < (TS >> 2); i += BD) smask[i] = 0u;
-    if (tid < 3) s_cnt[tid] = 0;
+    if (tid < 4) s_cnt[tid] = 0;
     cluster.sync();  // every CTA of the cluster runs and its sub-table is empty
     // Let the commit + copy kernel launch now: its CTAs warm L2 with their
     // request's state while this grid works, and wait for this grid's
@@ -115,7 +122,10 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
         const int16_t* map = a.lv.map + (long long)(q_ok ? q : 0) * d.L;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
-            const bool valid = q_ok && (lo + r * BD + tid < hi) && t[r] >= 0 && t[r] < limit;
+            const bool in_range = q_ok && (lo + r * BD + tid < hi) && t[r] >= 0 && t[r] < limit;
+            const bool extra = in_range && t[r] >= xstart;
+            const bool valid = in_range && !extra;  // goes through the index
+            if (extra) xbits |= 1u << r;
             code[r] = valid ? kMissPending : -1;
             if (d.dense) {  // dense index: the slot is one load away, no chain
                 e[r] = kEmpty;
@@ -275,13 +285,16 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
 
     // ---- 4. locations, miss lists, counters --------------------------------
     const long long wbase = (long long)b * d.C;
-    int n_hit = 0, n_inv = 0, n_miss = 0;
+    int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) {
         const int i = lo + r * BD + tid;
         if (i >= hi) continue;
         int loc;
-        if (code[r] >= 0) {
+        if ((xbits >> r) & 1u) {
+            loc = (int)((long long)d.R * (d.H + d.C) + (long long)q * d.E + t[r] % d.E);
+            ++n_ext;
+        } else if (code[r] >= 0) {
             loc = (int)(base + hrow[r]);
             ++n_hit;
         } else if (code[r] == -1) {
@@ -310,11 +323,13 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
     n_hit = __reduce_add_sync(0xffffffffu, n_hit);
     n_inv = __reduce_add_sync(0xffffffffu, n_inv);
     n_miss = __reduce_add_sync(0xffffffffu, n_miss);
+    n_ext = __reduce_add_sync(0xffffffffu, n_ext);
     if (lane == 0) {
         int* rc = cluster.map_shared_rank(s_cnt, 0);
         atomicAdd(&rc[0], n_hit);
         atomicAdd(&rc[1], n_inv);
         atomicAdd(&rc[2], n_miss);
+        if (n_ext) atomicAdd(&rc[3], n_ext);
     }
     cluster.sync();  // counters complete; no remote access after this point
     if (c == 0 && tid == 0) {
@@ -333,6 +348,7 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
             st[HS_STAT_DUP_MISSES] = n_miss - U;
             st[HS_STAT_UNIQUE_MISSES] = U;
             st[HS_STAT_INVALID] = n_inv;
+            st[HS_STAT_EXTRA] = s_cnt[3];
         }
         if (a.plan_count) a.plan_count[b] = U;
     }

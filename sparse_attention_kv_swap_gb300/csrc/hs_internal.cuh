@@ -50,6 +50,7 @@ struct Dims {
     int32_t hash_size;   // entries per request bank, power of two (>= 32); 0 if dense
     int32_t hash_shift;  // 32 - log2(hash_size)
     int32_t dense;       // 1: token -> slot index is the dense map, not the hash bank
+    int32_t E;           // extra-page rows per request (0 = no extra page)
 };
 
 struct LayerView {
@@ -60,7 +61,7 @@ struct LayerView {
     int32_t* phys;             // [R][H + C]
     int32_t* ctrl;             // [R][kCtrlWords]
     const uint8_t* host_pool;  // device mapping of the pinned pool [R][L][W]
-    uint8_t* device_kv;        // [R][H + C][W]
+    uint8_t* device_kv;        // [R * (H + C) + R * E][W]: hot + scratch rows, extra pages
 };
 
 struct Workspace {
@@ -124,6 +125,9 @@ cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaS
 cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
                                 int32_t B, int32_t C, int32_t W, const uint8_t* pool,
                                 uint8_t* kv, int ctas, cudaStream_t s);
+cudaError_t launch_append(const Dims& d, const LayerView& lv, uint8_t* host_pool,
+                          const int32_t* req, const int32_t* tok, const int32_t* seq_lens,
+                          const uint8_t* rows, int32_t n, uint32_t* status, cudaStream_t s);
 cudaError_t launch_reset(const Dims& d, uint8_t* state, const int32_t* rpi, int32_t n,
                          cudaStream_t s);
 cudaError_t launch_page_table(const int32_t* topk, const int32_t* seq_lens, int32_t B,

@@ -9,7 +9,6 @@ import torch
 
 import hs_workloads as W
 from checker import check_call
-from common import row_fn
 
 
 def map_consistent(st: dict) -> Optional[str]:
@@ -51,16 +50,21 @@ def bank_consistent(st: dict, dense: bool = False) -> Optional[str]:
 class ParityRun:
     def __init__(self, R: int, L: int, width: int, H: int, K: int, S_max: int, layers: int = 1,
                  max_batch: Optional[int] = None, pools=None, deferred: bool = False,
-                 dense: bool = False):
+                 dense: bool = False, extra_page: int = 0, own_pool: bool = False):
+        """own_pool: the oracle works on its own copy of the host pools (needed
+        once rows are appended, so that the library's write-back is compared
+        with the oracle's instead of being overwritten by it)."""
         self.deferred = deferred
         self.dense = dense
+        self.E = extra_page
         import sparse_attention_kv_swap_gb300 as pkg
         from oracle import Oracle
         from sparse_attention_kv_swap_gb300.cache import SwapInCache
         self.R, self.L, self.W, self.H, self.K, self.S_max = R, L, width, H, K, S_max
         self.C = S_max * K
         self.layers = layers
-        cfg = pkg.make_config(R, L, width, H, K, S_max, layers, max_batch, index_kind=int(dense))
+        cfg = pkg.make_config(R, L, width, H, K, S_max, layers, max_batch, index_kind=int(dense),
+                              extra_page_size=extra_page)
         if pools is None:
             pools = []
             for l in range(layers):
@@ -73,9 +77,36 @@ class ParityRun:
             t.zero_()
         if deferred:
             pkg.hs_set_defer_copy(self.cache.handle, True)
-        self.oracle = Oracle(R, L, width, H, K, S_max, layers)
-        self.mirror = [np.zeros((R * (H + self.C), width), dtype=np.uint8) for _ in range(layers)]
+        self.oracle = Oracle(R, L, width, H, K, S_max, layers, extra_page_size=extra_page)
+        self.mirror = [np.zeros((self.oracle.device_rows(), width), dtype=np.uint8)
+                       for _ in range(layers)]
+        self.opools = [p.numpy().copy() if own_pool else p.numpy() for p in pools]
         self.calls = 0
+
+    def append(self, req: np.ndarray, tok: np.ndarray, seq_lens: np.ndarray, rows: np.ndarray,
+               layer: int = 0, expect_skipped: int = 0) -> None:
+        """Write-back through the library and the oracle; compares the host
+        pool rows written and every device row."""
+        req = np.ascontiguousarray(req, dtype=np.int32)
+        tok = np.ascontiguousarray(tok, dtype=np.int32)
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        rows = np.ascontiguousarray(rows, dtype=np.uint8)
+        dev = lambda a: torch.from_numpy(a).cuda()
+        self.cache.append_rows(dev(req), dev(tok), dev(seq_lens), dev(rows), layer)
+        skipped = self.oracle.append_rows(layer, self.opools[layer], self.mirror[layer], req, tok,
+                                          seq_lens, rows)
+        torch.cuda.synchronize()
+        assert skipped == expect_skipped
+        rc, flags = self.cache.status()
+        import sparse_attention_kv_swap_gb300 as pkg
+        want = pkg.binding.HS_STATUS_BAD_APPEND if skipped else 0
+        assert flags == want, "append: device status flags %#x, expected %#x" % (flags, want)
+        ok = (req >= 0) & (req < self.R) & (tok >= 0) & (tok < np.minimum(seq_lens, self.L))
+        got = self.pools[layer].numpy()[req[ok], tok[ok]]
+        assert (got == self.opools[layer][req[ok], tok[ok]]).all(), "appended host rows differ"
+        diff = np.nonzero((self.cache.device_kv[layer].cpu().numpy() != self.mirror[layer])
+                          .any(axis=1))[0]
+        assert diff.size == 0, "append: %d device rows differ (first %d)" % (diff.size, diff[0])
 
     def gpu_state(self, layer: int, q: int) -> dict:
         return self.cache.export_request_state(layer, q)
@@ -100,7 +131,7 @@ class ParityRun:
                                 out["miss_count"], stream=side)
             torch.cuda.current_stream().wait_stream(side)
             plan = True
-        ref = self.oracle.swap_in(layer, self.pools[layer].numpy(), self.mirror[layer], rpi,
+        ref = self.oracle.swap_in(layer, self.opools[layer], self.mirror[layer], rpi,
                                   seq_lens, topk, want_plan=plan, num_threads=threads)
         torch.cuda.synchronize()
         g = {k: v.cpu().numpy() for k, v in out.items()}
@@ -138,9 +169,11 @@ class ParityRun:
                 idx = torch.from_numpy(np.asarray(locs, dtype=np.int64)).cuda()
                 return dev.index_select(0, idx).cpu().numpy()
 
+            opool = self.opools[layer]
             check_call(before, after, topk, rpi, seq_lens, self.L, self.H, self.C,
                        g["device_locs"], g["stats"], rows_at=rows_at,
-                       host_row=row_fn(layer, self.W))
+                       host_row=lambda q, toks: opool[q, np.asarray(toks)],
+                       extra_page=self.E, R=self.R)
         rc, flags = self.cache.status()
         assert flags == 0, "%s: device status flags %#x" % (tag, flags)
         return g

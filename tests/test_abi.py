@@ -29,12 +29,13 @@ def test_header_constants_match_binding():
     for name in ("HS_OK", "HS_ERR_INVALID_ARG", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                  "HS_ERR_DEVICE_STATUS", "HS_ERR_TIMEOUT", "HS_STATUS_BAD_REQUEST",
                  "HS_STATUS_DUPLICATE_REQUEST", "HS_STATUS_SEQ_LEN_CLAMPED",
-                 "HS_STATUS_PROBE_LIMIT", "HS_STATUS_TABLE_FULL", "HS_NUM_STATS"):
+                 "HS_STATUS_PROBE_LIMIT", "HS_STATUS_TABLE_FULL", "HS_STATUS_BAD_APPEND",
+                 "HS_NUM_STATS", "HS_MAX_EXTRA_PAGE"):
         assert int(consts[name], 0) == getattr(B, name), name
 
 
 def test_version_and_strings(lib):
-    assert pkg.hs_version() == 100
+    assert pkg.hs_version() == 10100
     assert pkg.hs_status_string(0) == "ok"
     assert "invalid" in pkg.hs_status_string(-1)
     assert pkg.hs_status_string(-99) == "unknown status"
@@ -135,3 +136,28 @@ def test_dense_index_config(lib):
     diff = pkg.hs_state_bytes(hashed) - pkg.hs_state_bytes(dense)
     assert abs(diff - (64 * 16384 * 8 - 64 * 32768 * 2)) <= 512
     assert pkg.hs_workspace_bytes(dense) == pkg.hs_workspace_bytes(hashed)
+
+
+def test_extra_page_config(lib):
+    """The extra page adds R * E device rows and is bounded."""
+    base = _cfg()
+    x = _cfg(extra_page_size=256)
+    assert pkg.hs_config_check(x) == B.HS_OK
+    assert (pkg.hs_device_kv_bytes(x) - pkg.hs_device_kv_bytes(base)
+            == base.num_requests * 256 * base.item_size_bytes)
+    assert pkg.hs_state_bytes(x) == pkg.hs_state_bytes(base)  # no policy state of its own
+    assert pkg.hs_config_check(_cfg(extra_page_size=-1)) == B.HS_ERR_INVALID_ARG
+    assert pkg.hs_config_check(_cfg(extra_page_size=B.HS_MAX_EXTRA_PAGE)) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(extra_page_size=B.HS_MAX_EXTRA_PAGE + 1)) == \
+        B.HS_ERR_UNSUPPORTED
+    # device rows must stay addressable by int32 locations
+    # (52428 requests of 32768 + 8192 rows are 32767 rows short of 2^31 - 1)
+    assert pkg.hs_config_check(_cfg(num_requests=52428, hot_buffer_size=32768,
+                                    extra_page_size=0)) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(num_requests=52428, hot_buffer_size=32768,
+                                    extra_page_size=1)) == B.HS_ERR_UNSUPPORTED
+
+
+def test_append_rows_argument_errors(lib):
+    """hs_append_rows rejects bad handles, layers, counts and unaligned rows on the host."""
+    assert lib.hs_append_rows(None, 0, None, None, None, None, 1, None) == B.HS_ERR_INVALID_ARG

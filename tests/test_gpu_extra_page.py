@@ -1,0 +1,114 @@
+"""Extra page and write-back on the GPU against the CPU oracle, bit for bit.
+
+The extra page is the request's newest, still-filling page: the gather
+serves a selected token on it from the page's device row before any
+hot-cache lookup (the multi-step swap report, 实现拆解 item 1).  Decode
+writes each new row back to the host pool (PR #20343 summary, 功能与动机)
+and to every device copy of it.  The decode loops below append one new
+token per request per step, rewrite older positions (a rolled-back
+speculative token), and resolve a selection biased towards the newest
+positions; every call compares locations, counters, policy state, the
+whole device buffer and the host rows written.
+"""
+import numpy as np
+import pytest
+
+import hs_workloads as W
+from gpu_harness import ParityRun
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode_loop(run, rng, R, L, K, S_max, E, steps, layers=1, rewrites=True):
+    n = rng.integers(L // 4, L // 2, size=R).astype(np.int32)
+    for layer in range(layers):
+        # prefill leaves the partial last page of every request on the device
+        for q in range(R):
+            toks = np.arange((n[q] - 1) // E * E if E else n[q] - 1, n[q], dtype=np.int32)
+            rows = rng.integers(0, 256, size=(toks.size, run.W), dtype=np.uint8)
+            run.append(np.full(toks.size, q, np.int32), toks, np.full(toks.size, n[q]), rows,
+                       layer=layer)
+    for step in range(steps):
+        n = np.minimum(n + 1, L).astype(np.int32)
+        B = int(rng.integers(1, R + 1))
+        rpi = rng.permutation(R)[:B].astype(np.int32)
+        for layer in range(layers):
+            # every request decodes a token; the call then selects for B of them
+            every = np.arange(R, dtype=np.int32)
+            req, tok = every, n - 1
+            if rewrites:
+                old = rng.integers(0, n).astype(np.int32)
+                keep = old != tok
+                req = np.concatenate([req, every[keep]])
+                tok = np.concatenate([tok, old[keep]])
+            rows = rng.integers(0, 256, size=(req.size, run.W), dtype=np.uint8)
+            run.append(req, tok, n[req], rows, layer=layer)
+            S = int(rng.integers(1, S_max + 1))
+            span = 3 * max(E, 1) + 8
+            recent = n[rpi][:, None, None] - 1 - rng.integers(0, span, size=(B, S, K))
+            spread = rng.integers(0, n[rpi][:, None, None], size=(B, S, K))
+            topk = np.where(rng.random((B, S, K)) < 0.4, recent, spread).astype(np.int32)
+            topk[rng.random(topk.shape) < 0.03] = -1
+            run.call(topk, rpi, n[rpi], layer=layer, properties=(step % 5 == 4))
+
+
+@pytest.mark.parametrize("dense", [False, True], ids=["hash", "dense"])
+@pytest.mark.parametrize("E", [1, 7, 64, 256])
+def test_decode_loop_extra_page(dense, E):
+    rng = np.random.default_rng(100 + E + 1000 * dense)
+    R, L, H, K, S_max = 6, 3000, 200, 300, 3
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max, dense=dense, extra_page=E, own_pool=True)
+    _decode_loop(run, rng, R, L, K, S_max, E, steps=14)
+
+
+def test_decode_loop_two_layers_overflow():
+    # small hot buffer: overflow every call; two layers keep separate rows
+    rng = np.random.default_rng(7)
+    R, L, H, K, S_max, E = 4, 1500, 40, 128, 4, 32
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max, layers=2, extra_page=E, own_pool=True)
+    _decode_loop(run, rng, R, L, K, S_max, E, steps=10, layers=2)
+
+
+def test_write_back_without_extra_page():
+    # E = 0: appended rows reach the host pool and the hot copies only
+    rng = np.random.default_rng(8)
+    R, L, H, K, S_max = 5, 2000, 150, 200, 2
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max, extra_page=0, own_pool=True)
+    _decode_loop(run, rng, R, L, K, S_max, 0, steps=10)
+
+
+def test_append_skips_out_of_range_entries():
+    rng = np.random.default_rng(9)
+    R, L, H, K, E = 4, 500, 32, 16, 8
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, 1, extra_page=E, own_pool=True)
+    req = np.array([0, 1, -1, 4, 2, 3, 3], np.int32)
+    tok = np.array([10, 499, 5, 5, -2, 50, 60], np.int32)
+    sl = np.array([11, 500, 10, 10, 10, 50, 61], np.int32)  # (3, 50): t == seq_len
+    rows = rng.integers(0, 256, size=(7, W.ROW_BYTES), dtype=np.uint8)
+    run.append(req, tok, sl, rows, expect_skipped=4)
+    # the valid ones were applied: select them through the extra page
+    # 10 is on the extra page [8, 11); 8 and 9, never appended, are not selected
+    topk = np.array([[[10, 3, 1, 0, 2, 4, 5, 6, 7, -1, 11, 12, 13, 14, 15, 20]]], np.int32)
+    run.call(topk, np.array([0], np.int32), np.array([11], np.int32), properties=True)
+
+
+def test_extra_page_full_size_c2():
+    """The 64-request, 32768-token workload with a 256-row extra page: the
+    newest token of every request is appended before each call."""
+    w = W.WORKLOADS["C2"]
+    E = 256
+    stream = W.TopkStream(w)
+    rpi = W.req_pool_indices(w)
+    sl = W.seq_lens(w)
+    rng = np.random.default_rng(12)
+    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, dense=True,
+                    extra_page=E, own_pool=True)
+    q = np.arange(w.batch, dtype=np.int32)
+    page = np.arange(w.seq_len - E, w.seq_len, dtype=np.int32)
+    run.append(np.repeat(q, E), np.tile(page, w.batch), np.full(w.batch * E, w.seq_len),
+               rng.integers(0, 256, size=(w.batch * E, w.row_bytes), dtype=np.uint8))
+    for c in range(5):
+        run.append(q, np.full(w.batch, w.seq_len - 1, np.int32), sl[q],
+                   rng.integers(0, 256, size=(w.batch, w.row_bytes), dtype=np.uint8))
+        g = run.call(stream.next_call(), rpi, sl, compare_rows=(c == 4), properties=(c == 4))
+        assert g["stats"][:, 8].sum() > 0  # the Zipf draws favour the newest positions
