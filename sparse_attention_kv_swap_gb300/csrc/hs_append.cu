@@ -8,12 +8,12 @@
 // position lies on it, and to the token's hot row when the token is
 // resident, so that every copy of (q, t) stays equal.
 //
-// One warp per entry.  Lane 0 validates the entry and resolves the two
-// device rows (extra row by arithmetic; hot row through the token -> slot
-// index and the position table); the warp then moves the W-byte row in
-// 16-byte vectors: one load from the caller's device rows, a store over the
-// host link into the mapped pool, and up to two stores into the device
-// buffer.
+// One warp per entry, in 16-byte vectors.  The warp loads the row while
+// lane 0 validates the entry; it then stores the host pool row (over the host
+// link, into the mapped pool) and the extra-page row, which follow from
+// (q, t) alone, and only then resolves the hot row through the token -> slot
+// index and the position table, so that the index lookups overlap the stores
+// in flight.
 #include "hs_internal.cuh"
 
 namespace hs {
@@ -64,33 +64,59 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendA
     const int i = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
     if (i >= a.n) return;
     const Dims& d = a.d;
-    long long host_row = -1, xrow = -1, hrow = -1;
-    if (lane == 0) {
-        const int q = __ldg(a.req + i), t = __ldg(a.tok + i), sl = __ldg(a.seq_lens + i);
-        const int limit = sl < d.L ? sl : d.L;
-        if (q < 0 || q >= d.R || t < 0 || t >= limit) {
-            atomicOr(a.status, HS_STATUS_BAD_APPEND);
-        } else {
-            host_row = (long long)q * d.L + t;
-            if (d.E > 0 && t >= (limit - 1) / d.E * d.E)
-                xrow = (long long)d.R * (d.H + d.C) + (long long)q * d.E + t % d.E;
-            const int slot = resident_slot(d, a.lv, q, t, a.status);
-            if (slot >= 0) {
-                const long long base = (long long)q * (d.H + d.C);
-                hrow = base + a.lv.phys[base + slot];
-            }
-        }
-    }
-    host_row = __shfl_sync(0xffffffffu, host_row, 0);
-    xrow = __shfl_sync(0xffffffffu, xrow, 0);
-    hrow = __shfl_sync(0xffffffffu, hrow, 0);
-    if (host_row < 0) return;
     const int vecs = d.W >> 4;
     const int4* src = reinterpret_cast<const int4*>(a.rows + (long long)i * d.W);
-    int4* dst_host = reinterpret_cast<int4*>(a.pool + host_row * d.W);
-    int4* dst_x = xrow >= 0 ? reinterpret_cast<int4*>(a.lv.device_kv + xrow * d.W) : nullptr;
+    // The first 64 vectors of the row (1 KB) are loaded at once, alongside
+    // the entry itself: neither depends on the other.
+    int4 x0 = make_int4(0, 0, 0, 0), x1 = x0;
+    if (lane < vecs) x0 = __ldg(src + lane);
+    if (lane + 32 < vecs) x1 = __ldg(src + lane + 32);
+    int q = 0, t = 0, limit = 0;
+    if (lane == 0) {
+        q = __ldg(a.req + i);
+        t = __ldg(a.tok + i);
+        const int sl = __ldg(a.seq_lens + i);
+        limit = sl < d.L ? sl : d.L;
+        if (q < 0 || q >= d.R || t < 0 || t >= limit) {
+            atomicOr(a.status, HS_STATUS_BAD_APPEND);
+            q = -1;
+        }
+    }
+    q = __shfl_sync(0xffffffffu, q, 0);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    limit = __shfl_sync(0xffffffffu, limit, 0);
+    if (q < 0) return;
+    // Host row and extra-page row follow from (q, t) alone: store them first.
+    int4* dst_host = reinterpret_cast<int4*>(a.pool + ((long long)q * d.L + t) * d.W);
+    int4* dst_x = nullptr;
+    if (d.E > 0 && t >= (limit - 1) / d.E * d.E)
+        dst_x = reinterpret_cast<int4*>(
+            a.lv.device_kv + ((long long)d.R * (d.H + d.C) + (long long)q * d.E + t % d.E) * d.W);
+    if (lane < vecs) {
+        dst_host[lane] = x0;
+        if (dst_x) dst_x[lane] = x0;
+    }
+    if (lane + 32 < vecs) {
+        dst_host[lane + 32] = x1;
+        if (dst_x) dst_x[lane + 32] = x1;
+    }
+    // The hot copy, if the token is resident: index lookup, then its row.
+    long long hrow = -1;
+    if (lane == 0) {
+        const int slot = resident_slot(d, a.lv, q, t, a.status);
+        if (slot >= 0) {
+            const long long base = (long long)q * (d.H + d.C);
+            hrow = base + a.lv.phys[base + slot];
+        }
+    }
+    hrow = __shfl_sync(0xffffffffu, hrow, 0);
     int4* dst_h = hrow >= 0 ? reinterpret_cast<int4*>(a.lv.device_kv + hrow * d.W) : nullptr;
-    for (int v = lane; v < vecs; v += 32) {
+    if (dst_h) {
+        if (lane < vecs) dst_h[lane] = x0;
+        if (lane + 32 < vecs) dst_h[lane + 32] = x1;
+    }
+    // Rows longer than 1 KB: the rest, vector by vector.
+    for (int v = lane + 64; v < vecs; v += 32) {
         const int4 x = __ldg(src + v);
         dst_host[v] = x;
         if (dst_x) dst_x[v] = x;

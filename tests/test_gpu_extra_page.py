@@ -112,3 +112,29 @@ def test_extra_page_full_size_c2():
                    rng.integers(0, 256, size=(w.batch, w.row_bytes), dtype=np.uint8))
         g = run.call(stream.next_call(), rpi, sl, compare_rows=(c == 4), properties=(c == 4))
         assert g["stats"][:, 8].sum() > 0  # the Zipf draws favour the newest positions
+
+
+def test_extra_page_covers_whole_sequence():
+    """E >= L: every valid entry is on the extra page; no lookup, no miss, and
+    the policy state changes only by its epoch."""
+    rng = np.random.default_rng(13)
+    R, L, H, K, E = 3, 200, 16, 64, 256
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, 2, extra_page=E, own_pool=True)
+    n = np.array([200, 57, 1], np.int32)
+    for q in range(R):
+        toks = np.arange(n[q], dtype=np.int32)
+        run.append(np.full(n[q], q, np.int32), toks, np.full(n[q], n[q]),
+                   rng.integers(0, 256, size=(n[q], W.ROW_BYTES), dtype=np.uint8))
+    for c in range(3):
+        topk = rng.integers(-5, 210, size=(R, 2, K)).astype(np.int32)
+        g = run.call(topk, np.arange(R, dtype=np.int32), n, properties=True)
+        assert (g["stats"][:, [0, 2, 3]] == 0).all()
+
+
+def test_extra_page_deferred_copy_plan():
+    """Deferred copy: the recorded miss plan holds the misses only; the extra
+    page needs no copy."""
+    rng = np.random.default_rng(14)
+    R, L, H, K, S_max, E = 4, 2000, 100, 200, 2, 64
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max, deferred=True, extra_page=E, own_pool=True)
+    _decode_loop(run, rng, R, L, K, S_max, E, steps=6, rewrites=False)

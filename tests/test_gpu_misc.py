@@ -125,7 +125,7 @@ def test_cuda_graph_replay_matches_direct():
     sl = torch.full((4,), 4000, dtype=torch.int32, device="cuda")
     topk_buf = torch.empty((4, 2, 256), dtype=torch.int32, device="cuda")
     out = {"device_locs": torch.empty((4, 2, 256), dtype=torch.int32, device="cuda"),
-           "stats": torch.empty((4, 8), dtype=torch.int32, device="cuda")}
+           "stats": torch.empty((4, B.HS_NUM_STATS), dtype=torch.int32, device="cuda")}
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         b.cache.swap_in(rpi, sl, topk_buf.zero_(), stats=True, out=out, stream=s)  # warm-up
