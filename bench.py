@@ -339,6 +339,7 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
         if k == 0:
             torch.cuda.synchronize()
             gate(torch, n)
+            torch.cuda.nvtx.range_push("decode_steps")  # lets a profiler select these launches
         flush.fill_(i & 0xFF)
         if k >= 0:
             ev[k][0].record(s)
@@ -348,6 +349,7 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
         cache.swap_in(rpi, sl, topk_all[i], 0, out={"device_locs": locs, "stats": stats[i]})
         if k >= 0:
             ev[k][2].record(s)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     rc, flags = cache.status()
     if flags:
@@ -366,6 +368,81 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
             "extra_entries_fraction": float(st[:, :, 8].sum() / (n * w.entries)),
             "unique_misses_per_step": float(st[:, :, 3].sum(axis=1).mean()),
             "gpu_launches_per_step": 3}
+
+
+def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers=4, n=10,
+                           copy_ctas=0):
+    """F2 in use: a `layers`-layer decode step, swap-in after swap-in on one
+    stream, against the deferred-copy protocol, where each layer's swap-in only
+    resolves and commits and its recorded miss plan is copied on a second
+    stream (hs_copy_planned), so that layer l's copy overlaps the resolve of
+    layer l + 1.  Every layer sees the same call stream (independent state per
+    layer) and shares the host pool."""
+    from sparse_attention_kv_swap_gb300.cache import SwapInCache
+    Bn, S, Kk, C = w.batch, w.steps, w.top_k, w.steps * w.top_k
+    cfg = pkg.make_config(Bn, w.seq_len, w.row_bytes, w.hot_buffer, Kk, S, layers,
+                          index_kind=1 if dense else 0)
+    seq = SwapInCache(cfg, host_pools=[pool] * layers, device=dev)
+    dfr = SwapInCache(cfg, host_pools=[pool] * layers, device=dev)
+    pkg.hs_set_defer_copy(dfr.handle, True)
+    if copy_ctas:
+        pkg.hs_set_copy_ctas(dfr.handle, copy_ctas)
+    rpi = torch.from_numpy(W.req_pool_indices(w)).to(dev)
+    sl = torch.from_numpy(W.seq_lens(w)).to(dev)
+    topk_all = torch.from_numpy(np.stack(calls[:PREROLL_CALLS + n])).to(dev)
+    locs = [torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev) for _ in range(layers)]
+    plans = [{"device_locs": locs[l],
+              "miss_src": torch.empty((Bn, C), dtype=torch.int64, device=dev),
+              "miss_dst": torch.empty((Bn, C), dtype=torch.int64, device=dev),
+              "miss_count": torch.empty(Bn, dtype=torch.int32, device=dev)}
+             for l in range(layers)]
+    s0 = torch.cuda.current_stream()
+    s1 = torch.cuda.Stream(device=dev)
+    done = [torch.cuda.Event() for _ in range(layers)]
+
+    def sequential(i):
+        for l in range(layers):
+            seq.swap_in(rpi, sl, topk_all[i], l, out={"device_locs": locs[l]})
+
+    def pipelined(i):
+        for l in range(layers):
+            dfr.swap_in(rpi, sl, topk_all[i], l, plan=True, out=plans[l])
+            done[l].record(s0)
+            s1.wait_event(done[l])
+            pkg.hs_copy_planned(dfr.handle, l, plans[l]["miss_src"], plans[l]["miss_dst"],
+                                plans[l]["miss_count"], stream=s1)
+        s0.wait_stream(s1)  # the step ends when every layer's rows are in
+
+    out = {}
+    for name, fn in (("sequential", sequential), ("deferred_pipelined", pipelined)):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for i in range(PREROLL_CALLS + n):
+            k = i - PREROLL_CALLS
+            if k == 0:
+                torch.cuda.synchronize()
+                gate(torch, 2 * n)
+                torch.cuda.nvtx.range_push(name + "_layers")
+            flush.fill_(i & 0xFF)
+            if k >= 0:
+                ev[k][0].record(s0)
+            fn(i)
+            if k >= 0:
+                ev[k][1].record(s0)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        out[name] = {"ms_per_step": ms, "value": layers * w.entries / (ms * 1e-3)}
+    for cache in (seq, dfr):
+        rc, flags = cache.status()
+        if flags:
+            raise RuntimeError("device status flags %#x in the deferred-copy pipeline" % flags)
+        cache.close()
+    out.update(layers=layers, steps=n, unit=UNIT,
+               speedup=out["sequential"]["ms_per_step"] / out["deferred_pipelined"]["ms_per_step"],
+               copy_ctas=copy_ctas or "default",
+               launch="direct launches through the C ABI; copies on a second stream")
+    return out
 
 
 def run_compare_sequential(args, w):
@@ -487,7 +564,7 @@ def main():
     n_e2e = min(K, 20)
     n_phase = min(K, 20)
     n_alt = min(K, 20)
-    total_calls = PREROLL_CALLS + Wm + 1 + K + n_phase + n_e2e + 2 + n_alt
+    total_calls = PREROLL_CALLS + Wm + 1 + K + n_phase + 2 * (n_e2e + 2) + n_alt
     stream_gen = W.TopkStream(w)
     calls = stream_gen.calls(total_calls)
     rpi_np, sl_np = W.req_pool_indices(w), W.seq_lens(w)
@@ -594,7 +671,7 @@ def main():
     st_timed = stats[base:base + K].cpu().numpy()
     # the other launch mode on the next calls of the stream, for comparison
     alt = "direct" if args.launch == "graph" else "graph"
-    abase = base + K + n_phase + n_e2e + 2
+    abase = base + K + n_phase + 2 * (n_e2e + 2)
     ev_alt = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n_alt)]
 
@@ -658,6 +735,32 @@ def main():
     e2e_ms = max_over_ranks(torch, e2e_ms, world, dev)
     h2d_bytes = n_in * 4
     d2h_bytes = locs_host.numel() * 4
+    # The same steps with no copy engine: over NVLink-C2C pinned host memory is
+    # device-addressable, so the call is given the pinned records and a pinned
+    # output, and its kernels read the inputs and write the locations across
+    # the link.  Same bytes each way.
+    zbase = ebase + n_e2e + 2
+    host_zc = torch.empty((n_e2e + 2, n_in), dtype=torch.int32).pin_memory()
+    for k in range(n_e2e + 2):
+        host_zc[k, :Bn * S * Kk] = torch.from_numpy(calls[zbase + k].reshape(-1))
+        host_zc[k, Bn * S * Kk:Bn * S * Kk + Bn] = torch.from_numpy(rpi_np)
+        host_zc[k, Bn * S * Kk + Bn:] = torch.from_numpy(sl_np)
+    zc_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e + 2)]
+    torch.cuda.synchronize()
+    gate(torch, n_e2e + 2)
+    for k in range(n_e2e + 2):
+        flush.fill_(k & 0xFF)
+        rec = host_zc[k]
+        zc_ev[k][0].record(s)
+        cache.swap_in(rec[Bn * S * Kk:Bn * S * Kk + Bn], rec[Bn * S * Kk + Bn:],
+                      rec[:Bn * S * Kk].view(Bn, S, Kk), 0, out={"device_locs": locs_host})
+        if page_out is not None:
+            cache.page_table(rec[:Bn * S * Kk].view(Bn, S, Kk), rec[Bn * S * Kk + Bn:],
+                             w.page_size, out=page_out)
+        zc_ev[k][1].record(s)
+    torch.cuda.synchronize()
+    zc_ms = max_over_ranks(torch, sum(a.elapsed_time(b) for a, b in zc_ev[2:]) / n_e2e, world,
+                           dev)
     rc, flags = cache.status()
     if flags:
         raise RuntimeError("device status flags %#x after the timed region" % flags)
@@ -670,6 +773,8 @@ def main():
                            float(stats[base:base + K, :, 3].float().mean()))
     decode = decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool,
                                     args.index == "dense", n=min(K, 20))
+    pipeline = deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool,
+                                      args.index == "dense", n=min(K, 10))
 
     # ---- roofline bookkeeping (algorithmic bytes) ----
     U_phase = st_phase[:, :, 3].sum(axis=1).astype(np.float64)
@@ -696,7 +801,13 @@ def main():
             if args.launch == "graph" else "direct launches through the C ABI")),
         "e2e": {"value": whole_job_rate(w.entries, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
-                "ms_per_step": e2e_ms, **e2e_parts},
+                "ms_per_step": e2e_ms, **e2e_parts,
+                "zero_copy": {"value": whole_job_rate(w.entries, world, zc_ms), "unit": UNIT,
+                              "ms_per_step": zc_ms, "h2d_bytes_per_step": int(h2d_bytes),
+                              "d2h_bytes_per_step": int(d2h_bytes),
+                              "how": "pinned host input record and pinned output passed to "
+                                     "the call; the kernels read and write them over "
+                                     "NVLink-C2C (no copy-engine transfer)"}},
         "gpu_launches": K * n_kernels,
         "roofline": {"kernel": "commit_copy_kernel (commit CTAs + miss-row copy CTAs)",
                      "bound": "host_link", "achieved": achieved_copy, "peak": h2d_peak,
@@ -728,6 +839,7 @@ def main():
         },
         "copy_ceiling": ceiling,
         "decode_step_extra_page": decode,
+        "deferred_copy_pipeline": pipeline,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -20,6 +20,9 @@
  *
  * Conventions for every call:
  *  - Pointers named *_dev are device pointers; *_host are host pointers.
+ *    A device pointer may also address mapped pinned host memory (with
+ *    unified addressing, the pinned buffer's own address): the kernels then
+ *    read or write it across the host link, e.g. NVLink-C2C on Grace.
  *    The caller owns every buffer (pinned host pool, device KV buffers,
  *    state, workspace, inputs, outputs).  The library owns only the small
  *    host handle `hs_state`.

@@ -138,3 +138,24 @@ def test_extra_page_deferred_copy_plan():
     R, L, H, K, S_max, E = 4, 2000, 100, 200, 2, 64
     run = ParityRun(R, L, W.ROW_BYTES, H, K, S_max, deferred=True, extra_page=E, own_pool=True)
     _decode_loop(run, rng, R, L, K, S_max, E, steps=6, rewrites=False)
+
+
+def test_largest_extra_page():
+    """E = HS_MAX_EXTRA_PAGE (65536) on 70000-token requests: the extra page
+    is [65536, n) once n passes 65536 and the whole sequence before that."""
+    import sparse_attention_kv_swap_gb300 as pkg
+    E = pkg.binding.HS_MAX_EXTRA_PAGE
+    rng = np.random.default_rng(15)
+    R, L, H, K = 2, 70000, 64, 512
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, 1, extra_page=E, own_pool=True)
+    n = np.array([70000, 65536], np.int32)
+    for q in range(R):
+        toks = np.arange((n[q] - 1) // E * E, n[q], dtype=np.int32)
+        run.append(np.full(toks.size, q, np.int32), toks, np.full(toks.size, n[q]),
+                   rng.integers(0, 256, size=(toks.size, W.ROW_BYTES), dtype=np.uint8))
+    for c in range(3):
+        recent = n[:, None, None] - 1 - rng.integers(0, 6000, size=(R, 1, K))
+        topk = np.where(rng.random((R, 1, K)) < 0.5, recent,
+                        rng.integers(0, n[:, None, None], size=(R, 1, K))).astype(np.int32)
+        g = run.call(topk, np.arange(R, dtype=np.int32), n, properties=True)
+        assert g["stats"][1, 8] == int(((topk[1] >= 0) & (topk[1] < n[1])).sum())  # all extra

@@ -148,3 +148,30 @@ def test_cuda_graph_replay_matches_direct():
         sa, sb = a.gpu_state(0, q), b.gpu_state(0, q)
         for k in ("tok", "ep", "phys"):
             assert (sa[k] == sb[k]).all()
+
+
+def test_pinned_host_inputs_and_outputs_match_device_buffers():
+    """Pinned host memory is device-addressable (mapped, unified addresses):
+    the call given pinned host inputs and outputs, read and written by its
+    kernels across the host link, gives what the same call on device buffers
+    gives."""
+    rng = np.random.default_rng(31)
+    a = ParityRun(4, 3000, W.ROW_BYTES, 128, 256, 2, dense=True)
+    b = ParityRun(4, 3000, W.ROW_BYTES, 128, 256, 2, dense=True, pools=a.pools)
+    for c in range(4):
+        topk = rng.integers(-3, 3000, size=(4, 2, 256)).astype(np.int32)
+        rpi = rng.permutation(4).astype(np.int32)
+        sl = rng.integers(2000, 3001, size=4).astype(np.int32)
+        ga = a.call(topk, rpi, sl)
+        pin = lambda x: torch.from_numpy(x).pin_memory()
+        out = {"device_locs": torch.empty((4, 2, 256), dtype=torch.int32).pin_memory(),
+               "stats": torch.empty((4, B.HS_NUM_STATS), dtype=torch.int32).pin_memory()}
+        b.cache.swap_in(pin(rpi), pin(sl), pin(topk), 0, out=out)
+        torch.cuda.synchronize()
+        assert (out["device_locs"].numpy() == ga["device_locs"]).all()
+        assert (out["stats"].numpy() == ga["stats"]).all()
+        for q in range(4):
+            sa, sb = a.gpu_state(0, q), b.gpu_state(0, q)
+            for k in ("tok", "ep", "phys"):
+                assert (sa[k] == sb[k]).all()
+    assert (a.cache.device_kv[0].cpu() == b.cache.device_kv[0].cpu()).all()
