@@ -51,6 +51,10 @@ NCU_TRAFFIC = {("C2", "dense"): {"commit_copy_host_link_bytes": 347275 * 32,
                                 "gather_dram_bytes": 5837568}}
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
+# Untimed steps run right after each gate, before the timed ones: on GB300
+# the first step after the gate's idle wait ran about twice as slow as the
+# rest, every time.
+PRIMER_STEPS = 2
 FLUSH_BYTES = 256 << 20
 
 
@@ -88,7 +92,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 20):
+    def __init__(self, gpu_index: int, interval_ms: int = 200):
         self.samples = []
         self.proc = None
         self.gpu = gpu_index
@@ -110,6 +114,13 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_first(self, timeout: float = 5.0):
+        """Returns once the first sample has arrived: nvidia-smi's start-up
+        (which slowed the GPU's first steps when it overlapped them) is over."""
+        t_end = time.time() + timeout
+        while self.proc is not None and not self.samples and time.time() < t_end:
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is not None:
@@ -336,9 +347,10 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     for i in range(PREROLL_CALLS + n):
         k = i - PREROLL_CALLS
-        if k == 0:
+        if k == -PRIMER_STEPS:
             torch.cuda.synchronize()
-            gate(torch, n)
+            gate(torch, n + PRIMER_STEPS)
+        if k == 0:
             torch.cuda.nvtx.range_push("decode_steps")  # lets a profiler select these launches
         flush.fill_(i & 0xFF)
         if k >= 0:
@@ -419,9 +431,10 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
               for _ in range(n)]
         for i in range(PREROLL_CALLS + n):
             k = i - PREROLL_CALLS
-            if k == 0:
+            if k == -PRIMER_STEPS:
                 torch.cuda.synchronize()
-                gate(torch, 2 * n)
+                gate(torch, 2 * (n + PRIMER_STEPS))
+            if k == 0:
                 torch.cuda.nvtx.range_push(name + "_layers")
             flush.fill_(i & 0xFF)
             if k >= 0:
@@ -564,7 +577,8 @@ def main():
     n_e2e = min(K, 20)
     n_phase = min(K, 20)
     n_alt = min(K, 20)
-    total_calls = PREROLL_CALLS + Wm + 1 + K + n_phase + 2 * (n_e2e + 2) + n_alt
+    total_calls = (PREROLL_CALLS + Wm + 1 + K + n_phase + 2 * (n_e2e + 2) + n_alt
+                   + 3 * PRIMER_STEPS)
     stream_gen = W.TopkStream(w)
     calls = stream_gen.calls(total_calls)
     rpi_np, sl_np = W.req_pool_indices(w), W.seq_lens(w)
@@ -647,15 +661,19 @@ def main():
     # ---- timed region: K steps, per-step events, L2 flush between steps ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
+    primer_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(PRIMER_STEPS)]
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.wait_first()
     time.sleep(0.05)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    base = PREROLL_CALLS + Wm + 1  # after the graph warm-up call
-    gate(torch, K)
+    base = PREROLL_CALLS + Wm + 1 + PRIMER_STEPS  # after the graph warm-up and primer calls
+    gate(torch, K + PRIMER_STEPS)
+    run_steps(base - PRIMER_STEPS, PRIMER_STEPS, args.launch, primer_ev)
     torch.cuda.nvtx.range_push("timed_steps")  # lets a profiler select these launches
     run_steps(base, K, args.launch, ev)
     torch.cuda.nvtx.range_pop()
@@ -671,7 +689,7 @@ def main():
     st_timed = stats[base:base + K].cpu().numpy()
     # the other launch mode on the next calls of the stream, for comparison
     alt = "direct" if args.launch == "graph" else "graph"
-    abase = base + K + n_phase + 2 * (n_e2e + 2)
+    abase = base + K + PRIMER_STEPS + n_phase + 2 * (n_e2e + 2) + PRIMER_STEPS
     ev_alt = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n_alt)]
 
@@ -681,8 +699,11 @@ def main():
     e_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
     for e in e_m:  # torch creates the CUDA event at its first record
         e.record(s)
-    pbase = base + K
-    gate(torch, n_phase)
+    pbase = base + K + PRIMER_STEPS
+    gate(torch, n_phase + PRIMER_STEPS)
+    for i in range(base + K, pbase):
+        flush.fill_(i & 0xFF)
+        step(i, topk_all[i])
     for k in range(n_phase):
         flush.fill_(k & 0xFF)
         pkg.hs_set_phase_event(cache.handle, e_m[k])
@@ -765,7 +786,8 @@ def main():
     if flags:
         raise RuntimeError("device status flags %#x after the timed region" % flags)
     torch.cuda.synchronize()
-    gate(torch, n_alt)
+    gate(torch, n_alt + PRIMER_STEPS)
+    run_steps(abase - PRIMER_STEPS, PRIMER_STEPS, alt, primer_ev)
     run_steps(abase, n_alt, alt, ev_alt)
     torch.cuda.synchronize()
     alt_ms = sum(a.elapsed_time(b) for a, b in ev_alt) / n_alt
