@@ -51,10 +51,12 @@ NCU_TRAFFIC = {("C2", "dense"): {"commit_copy_host_link_bytes": 347275 * 32,
                                 "gather_dram_bytes": 5837568}}
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
-# Untimed steps run right after each gate, before the timed ones: on GB300
-# the first step after the gate's idle wait ran about twice as slow as the
-# rest, every time.
-PRIMER_STEPS = 2
+# Untimed steps run right after each gate, before the timed ones.  On GB300
+# the first step after the gate always ran about twice as slow as the rest,
+# and about one run in five began with a slow stretch of up to ~15 ms (steps
+# up to 10x slow, decaying), host enqueue well ahead of the GPU throughout;
+# 16 primer steps (2.5 ms of C2 work) absorbed it in every run we made.
+PRIMER_STEPS = 16
 FLUSH_BYTES = 256 << 20
 
 
@@ -337,16 +339,17 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
                       pre_rows)
     new_tok = torch.full((Bn,), L - 1, dtype=torch.int32, device=dev)
     new_len = torch.full((Bn,), L, dtype=torch.int32, device=dev)
-    rows = torch.randint(0, 256, (n + PREROLL_CALLS, Bn, Wr), dtype=torch.uint8, device=dev,
+    lead = PREROLL_CALLS + PRIMER_STEPS  # untimed calls before the timed ones
+    rows = torch.randint(0, 256, (n + lead, Bn, Wr), dtype=torch.uint8, device=dev,
                          generator=gen)
-    topk_all = torch.from_numpy(np.stack(calls[:PREROLL_CALLS + n])).to(dev)
+    topk_all = torch.from_numpy(np.stack(calls[:lead + n])).to(dev)
     locs = torch.empty((Bn, w.steps, w.top_k), dtype=torch.int32, device=dev)
-    stats = torch.zeros((PREROLL_CALLS + n, Bn, pkg.binding.HS_NUM_STATS), dtype=torch.int32,
+    stats = torch.zeros((lead + n, Bn, pkg.binding.HS_NUM_STATS), dtype=torch.int32,
                         device=dev)
     s = torch.cuda.current_stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-    for i in range(PREROLL_CALLS + n):
-        k = i - PREROLL_CALLS
+    for i in range(lead + n):
+        k = i - lead
         if k == -PRIMER_STEPS:
             torch.cuda.synchronize()
             gate(torch, n + PRIMER_STEPS)
@@ -369,7 +372,7 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
     app = [e[0].elapsed_time(e[1]) for e in ev]
     swp = [e[1].elapsed_time(e[2]) for e in ev]
     pair = [e[0].elapsed_time(e[2]) for e in ev]
-    st = stats[PREROLL_CALLS:].cpu().numpy()
+    st = stats[lead:].cpu().numpy()
     ms = statistics.mean(pair)
     cache.close()
     return {"extra_page_size": E, "steps": n, "launch": "direct launches through the C ABI",
@@ -401,7 +404,8 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
         pkg.hs_set_copy_ctas(dfr.handle, copy_ctas)
     rpi = torch.from_numpy(W.req_pool_indices(w)).to(dev)
     sl = torch.from_numpy(W.seq_lens(w)).to(dev)
-    topk_all = torch.from_numpy(np.stack(calls[:PREROLL_CALLS + n])).to(dev)
+    lead = PREROLL_CALLS + PRIMER_STEPS  # untimed calls before the timed ones
+    topk_all = torch.from_numpy(np.stack(calls[:lead + n])).to(dev)
     locs = [torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev) for _ in range(layers)]
     plans = [{"device_locs": locs[l],
               "miss_src": torch.empty((Bn, C), dtype=torch.int64, device=dev),
@@ -429,8 +433,8 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
     for name, fn in (("sequential", sequential), ("deferred_pipelined", pipelined)):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n)]
-        for i in range(PREROLL_CALLS + n):
-            k = i - PREROLL_CALLS
+        for i in range(lead + n):
+            k = i - lead
             if k == -PRIMER_STEPS:
                 torch.cuda.synchronize()
                 gate(torch, 2 * (n + PRIMER_STEPS))
@@ -523,6 +527,9 @@ def run_compare_sequential(args, w):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             with torch.cuda.stream(stream):  # replay runs on the current stream
+                # a 0.1 ms device-side hold so that the graph launch is queued
+                # before event `a` runs (too short for the clocks to drop)
+                torch.cuda._sleep(int(2e5))
                 a.record(stream)
                 g.replay()
                 b.record(stream)
@@ -577,7 +584,7 @@ def main():
     n_e2e = min(K, 20)
     n_phase = min(K, 20)
     n_alt = min(K, 20)
-    total_calls = (PREROLL_CALLS + Wm + 1 + K + n_phase + 2 * (n_e2e + 2) + n_alt
+    total_calls = (PREROLL_CALLS + Wm + 1 + K + n_phase + 2 * (n_e2e + PRIMER_STEPS) + n_alt
                    + 3 * PRIMER_STEPS)
     stream_gen = W.TopkStream(w)
     calls = stream_gen.calls(total_calls)
@@ -610,6 +617,9 @@ def main():
         cache.swap_in(rpi, sl, topk, 0, out={"device_locs": locs, "stats": stats[i]})
         if page_out is not None:
             cache.page_table(topk, sl, w.page_size, out=page_out)
+
+    # the host-link peak first, far from any timed region
+    h2d_peak = measure_h2d_peak(torch, dev)
 
     # pre-roll and warm-up
     for i in range(PREROLL_CALLS + Wm):
@@ -653,7 +663,6 @@ def main():
     run_steps(PREROLL_CALLS + Wm, 1, "graph", warm_ev)
     torch.cuda.synchronize()
 
-    h2d_peak = measure_h2d_peak(torch, dev)
     peaks = read_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     hbm_src = "MEASURED_PEAKS.json hbm_gbs (measured)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
@@ -689,7 +698,7 @@ def main():
     st_timed = stats[base:base + K].cpu().numpy()
     # the other launch mode on the next calls of the stream, for comparison
     alt = "direct" if args.launch == "graph" else "graph"
-    abase = base + K + PRIMER_STEPS + n_phase + 2 * (n_e2e + 2) + PRIMER_STEPS
+    abase = base + K + PRIMER_STEPS + n_phase + 2 * (n_e2e + PRIMER_STEPS) + PRIMER_STEPS
     ev_alt = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n_alt)]
 
@@ -720,11 +729,11 @@ def main():
     # ---- e2e: host buffers through the same C ABI call ----
     # Each step's inputs sit in one pinned host record [top-k | slots | lengths]
     # and go over in one copy; the locations come back into pinned memory.
-    # Two untimed steps first touch the host buffers.
+    # PRIMER_STEPS untimed steps come first (they also touch the host buffers).
     ebase = pbase + n_phase
     n_in = Bn * S * Kk + 2 * Bn
-    host_in = torch.empty((n_e2e + 2, n_in), dtype=torch.int32).pin_memory()
-    for k in range(n_e2e + 2):
+    host_in = torch.empty((n_e2e + PRIMER_STEPS, n_in), dtype=torch.int32).pin_memory()
+    for k in range(n_e2e + PRIMER_STEPS):
         host_in[k, :Bn * S * Kk] = torch.from_numpy(calls[ebase + k].reshape(-1))
         host_in[k, Bn * S * Kk:Bn * S * Kk + Bn] = torch.from_numpy(rpi_np)
         host_in[k, Bn * S * Kk + Bn:] = torch.from_numpy(sl_np)
@@ -733,10 +742,10 @@ def main():
     topk_dev = dev_in[:Bn * S * Kk].view(Bn, S, Kk)
     rpi_dev = dev_in[Bn * S * Kk:Bn * S * Kk + Bn]
     sl_dev = dev_in[Bn * S * Kk + Bn:]
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_e2e + 2)]
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_e2e + PRIMER_STEPS)]
     torch.cuda.synchronize()
-    gate(torch, n_e2e + 2)
-    for k in range(n_e2e + 2):
+    gate(torch, n_e2e + PRIMER_STEPS)
+    for k in range(n_e2e + PRIMER_STEPS):
         flush.fill_(k & 0xFF)
         e2e_ev[k][0].record(s)
         dev_in.copy_(host_in[k], non_blocking=True)
@@ -748,7 +757,7 @@ def main():
         locs_host.copy_(locs, non_blocking=True)
         e2e_ev[k][3].record(s)
     torch.cuda.synchronize()
-    e2e_ev = e2e_ev[2:]
+    e2e_ev = e2e_ev[PRIMER_STEPS:]
     e2e_ms = sum(ev[0].elapsed_time(ev[3]) for ev in e2e_ev) / n_e2e
     e2e_parts = {name: statistics.median(ev[i].elapsed_time(ev[i + 1]) for ev in e2e_ev)
                  for i, name in enumerate(("h2d_ms_median", "swap_in_ms_median",
@@ -760,16 +769,16 @@ def main():
     # device-addressable, so the call is given the pinned records and a pinned
     # output, and its kernels read the inputs and write the locations across
     # the link.  Same bytes each way.
-    zbase = ebase + n_e2e + 2
-    host_zc = torch.empty((n_e2e + 2, n_in), dtype=torch.int32).pin_memory()
-    for k in range(n_e2e + 2):
+    zbase = ebase + n_e2e + PRIMER_STEPS
+    host_zc = torch.empty((n_e2e + PRIMER_STEPS, n_in), dtype=torch.int32).pin_memory()
+    for k in range(n_e2e + PRIMER_STEPS):
         host_zc[k, :Bn * S * Kk] = torch.from_numpy(calls[zbase + k].reshape(-1))
         host_zc[k, Bn * S * Kk:Bn * S * Kk + Bn] = torch.from_numpy(rpi_np)
         host_zc[k, Bn * S * Kk + Bn:] = torch.from_numpy(sl_np)
-    zc_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e + 2)]
+    zc_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e + PRIMER_STEPS)]
     torch.cuda.synchronize()
-    gate(torch, n_e2e + 2)
-    for k in range(n_e2e + 2):
+    gate(torch, n_e2e + PRIMER_STEPS)
+    for k in range(n_e2e + PRIMER_STEPS):
         flush.fill_(k & 0xFF)
         rec = host_zc[k]
         zc_ev[k][0].record(s)
@@ -780,7 +789,7 @@ def main():
                              w.page_size, out=page_out)
         zc_ev[k][1].record(s)
     torch.cuda.synchronize()
-    zc_ms = max_over_ranks(torch, sum(a.elapsed_time(b) for a, b in zc_ev[2:]) / n_e2e, world,
+    zc_ms = max_over_ranks(torch, sum(a.elapsed_time(b) for a, b in zc_ev[PRIMER_STEPS:]) / n_e2e, world,
                            dev)
     rc, flags = cache.status()
     if flags:

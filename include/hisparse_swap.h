@@ -243,7 +243,10 @@ int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
 
 /* Returns requests to the empty state in every layer (use when a request
  * slot is given to a new sequence; order it after the previous user's last
- * call and before the new user's first call on `stream`). */
+ * call and before the new user's first call on `stream`).  Only policy
+ * state is reset: KV rows (host pool, device buffer, extra page) are left as
+ * they are, and the new sequence's rows arrive through its own prefill and
+ * hs_append_rows. */
 int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t n,
                       void* stream);
 
