@@ -94,7 +94,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 200):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.samples = []
         self.proc = None
         self.gpu = gpu_index
