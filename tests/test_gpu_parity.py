@@ -184,3 +184,42 @@ def test_workload_full_size_dense_index(name):
     for c in range(6):
         run.call(stream.next_call(), rpi, sl, compare_rows=(c == 5),
                  properties=(name == "C4" and c == 5))
+
+
+@pytest.mark.parametrize("name", ["C2", "C3"])
+def test_full_size_graph_replay_as_benchmarked(name):
+    """The benchmark's launch configuration at full size: dense index, one
+    swap-in captured in a CUDA graph on a side stream and replayed with each
+    call's top-k staged into the graph's input buffer."""
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    w = W.WORKLOADS[name]
+    stream = W.TopkStream(w)
+    rpi, sl = W.req_pool_indices(w), W.seq_lens(w)
+    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, dense=True)
+    run.call(stream.next_call(), rpi, sl, compare_rows=False)  # also sets kernel attributes
+    dev = torch.device("cuda")
+    rpi_t, sl_t = torch.from_numpy(rpi).to(dev), torch.from_numpy(sl).to(dev)
+    topk_buf = torch.empty((w.batch, w.steps, w.top_k), dtype=torch.int32, device=dev)
+    out = {"device_locs": torch.empty_like(topk_buf),
+           "stats": torch.empty((w.batch, pkg.binding.HS_NUM_STATS), dtype=torch.int32,
+                                device=dev)}
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        run.cache.swap_in(rpi_t, sl_t, topk_buf, 0, out=out, stream=side)
+    for c in range(4):
+        topk = stream.next_call()
+        topk_buf.copy_(torch.from_numpy(topk))
+        graph.replay()
+        ref = run.oracle.swap_in(0, run.opools[0], run.mirror[0], rpi, sl, topk, num_threads=8)
+        torch.cuda.synchronize()
+        assert (out["device_locs"].cpu().numpy() == ref["locs"]).all(), "call %d: locations" % c
+        assert (out["stats"].cpu().numpy() == ref["stats"]).all(), "call %d: counters" % c
+        for q in rpi.tolist():
+            g, o = run.gpu_state(0, q), run.oracle.request_state(0, q)
+            for k in ("tok", "ep", "phys"):
+                assert (g[k] == o[k]).all(), "call %d q=%d: %s" % (c, q, k)
+    got = run.cache.device_kv[0].cpu().numpy()
+    assert (got == run.mirror[0]).all(), "device rows differ after the replays"
+    assert run.cache.status() == (0, 0)
