@@ -613,10 +613,20 @@ def main():
                     "token_page": torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)}
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    # The page table depends on the top-k and lengths only, so it runs on a
+    # second stream beside the swap-in and joins it at the end of the step.
+    pt_stream = torch.cuda.Stream(device=dev)
+
+    def page_table_beside(topk, lens, origin):
+        pt_stream.wait_stream(origin)
+        cache.page_table(topk, lens, w.page_size, out=page_out, stream=pt_stream)
+
     def step(i, topk):
+        if page_out is not None:
+            page_table_beside(topk, sl, s)
         cache.swap_in(rpi, sl, topk, 0, out={"device_locs": locs, "stats": stats[i]})
         if page_out is not None:
-            cache.page_table(topk, sl, w.page_size, out=page_out)
+            s.wait_stream(pt_stream)
 
     # the host-link peak first, far from any timed region
     h2d_peak = measure_h2d_peak(torch, dev)
@@ -636,10 +646,12 @@ def main():
     side = torch.cuda.Stream()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=side):
+        if page_out is not None:
+            page_table_beside(topk_buf, sl, side)
         cache.swap_in(rpi, sl, topk_buf, 0, out={"device_locs": locs, "stats": stats_buf},
                       stream=side)
         if page_out is not None:
-            cache.page_table(topk_buf, sl, w.page_size, out=page_out, stream=side)
+            side.wait_stream(pt_stream)
 
     def run_steps(first, n, mode, events):
         """n steps from call `first` on, each between its own pair of events."""
@@ -750,9 +762,11 @@ def main():
         e2e_ev[k][0].record(s)
         dev_in.copy_(host_in[k], non_blocking=True)
         e2e_ev[k][1].record(s)
+        if page_out is not None:
+            page_table_beside(topk_dev, sl_dev, s)
         cache.swap_in(rpi_dev, sl_dev, topk_dev, 0, out={"device_locs": locs})
         if page_out is not None:
-            cache.page_table(topk_dev, sl_dev, w.page_size, out=page_out)
+            s.wait_stream(pt_stream)
         e2e_ev[k][2].record(s)
         locs_host.copy_(locs, non_blocking=True)
         e2e_ev[k][3].record(s)
@@ -782,11 +796,12 @@ def main():
         flush.fill_(k & 0xFF)
         rec = host_zc[k]
         zc_ev[k][0].record(s)
+        if page_out is not None:
+            page_table_beside(rec[:Bn * S * Kk].view(Bn, S, Kk), rec[Bn * S * Kk + Bn:], s)
         cache.swap_in(rec[Bn * S * Kk:Bn * S * Kk + Bn], rec[Bn * S * Kk + Bn:],
                       rec[:Bn * S * Kk].view(Bn, S, Kk), 0, out={"device_locs": locs_host})
         if page_out is not None:
-            cache.page_table(rec[:Bn * S * Kk].view(Bn, S, Kk), rec[Bn * S * Kk + Bn:],
-                             w.page_size, out=page_out)
+            s.wait_stream(pt_stream)
         zc_ev[k][1].record(s)
     torch.cuda.synchronize()
     zc_ms = max_over_ranks(torch, sum(a.elapsed_time(b) for a, b in zc_ev[PRIMER_STEPS:]) / n_e2e, world,
