@@ -223,3 +223,15 @@ def test_full_size_graph_replay_as_benchmarked(name):
     got = run.cache.device_kv[0].cpu().numpy()
     assert (got == run.mirror[0]).all(), "device rows differ after the replays"
     assert run.cache.status() == (0, 0)
+
+
+@pytest.mark.parametrize("B,S,K", [(160, 1, 2048), (100, 4, 2048), (300, 2, 64)])
+def test_batches_wider_than_the_gpu(B, S, K):
+    """More requests than SMs: single-CTA gathers with 2 entries per thread
+    (160 x 2048), 2-CTA clusters in more than one wave (100 x 4 x 2048), and
+    many small requests (300 x 2 x 64)."""
+    rng = np.random.default_rng(B + S)
+    R, L, H = B + 7, 2500, 512
+    run = ParityRun(R, L, W.ROW_BYTES, H, K, S, max_batch=B)
+    for topk, rpi, sl in _rand_calls(rng, R, L, K, S, B, 4):
+        run.call(topk, rpi, sl, properties=False)
