@@ -35,6 +35,7 @@ HS_STATUS_BAD_APPEND = 0x20
 HS_INDEX_HASH = 0
 HS_INDEX_DENSE = 1
 
+HS_STAT_EXTRA = 8
 HS_NUM_STATS = 9
 STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "evicted",
               "overflow", "invalid", "extra")

@@ -159,3 +159,42 @@ def test_largest_extra_page():
                         rng.integers(0, n[:, None, None], size=(R, 1, K))).astype(np.int32)
         g = run.call(topk, np.arange(R, dtype=np.int32), n, properties=True)
         assert g["stats"][1, 8] == int(((topk[1] >= 0) & (topk[1] < n[1])).sum())  # all extra
+
+
+def test_noalloc_entry_with_extra_page_matches_swap_in():
+    """hs_swap_in_noalloc serves the extra page exactly as hs_swap_in does."""
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    from sparse_attention_kv_swap_gb300 import binding as B
+    from sparse_attention_kv_swap_gb300.cache import SwapInCache
+    R, L, H, K, S, E = 4, 2000, 100, 200, 2, 32
+    cfg = pkg.make_config(R, L, W.ROW_BYTES, H, K, S, extra_page_size=E)
+    pool = torch.empty((R, L, W.ROW_BYTES), dtype=torch.uint8, pin_memory=True)
+    W.fill_host_pool(pool.numpy(), 0)
+    a, b = SwapInCache(cfg, host_pools=[pool]), SwapInCache(cfg, host_pools=[pool])
+    for c in (a, b):
+        c.device_kv[0].zero_()
+    rng = np.random.default_rng(16)
+    rpi = torch.tensor([2, 0, 3], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([2000, 1500, 777], dtype=torch.int32, device="cuda")
+    for call in range(3):
+        topk_np = rng.integers(-2, L, size=(3, S, K)).astype(np.int32)
+        topk_np[:, :, :20] = (sl.cpu().numpy()[:, None, None] - 1
+                              - rng.integers(0, 2 * E, size=(3, S, 20)))
+        topk = torch.from_numpy(topk_np).cuda()
+        outs = []
+        for c, fn in ((a, B.hs_swap_in), (b, B.hs_swap_in_noalloc)):
+            o = {"device_locs": torch.empty((3, S, K), dtype=torch.int32, device="cuda"),
+                 "stats": torch.empty((3, B.HS_NUM_STATS), dtype=torch.int32, device="cuda")}
+            fn(c.handle, rpi, sl, topk, 0, o["device_locs"], o["stats"])
+            outs.append(o)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[0]["device_locs"], outs[1]["device_locs"])
+        assert torch.equal(outs[0]["stats"], outs[1]["stats"])
+        assert int(outs[0]["stats"][:, B.HS_STAT_EXTRA].sum()) > 0
+    for q in (0, 2, 3):
+        sa, sb = a.export_request_state(0, q), b.export_request_state(0, q)
+        for k in ("tok", "ep", "phys"):
+            assert (sa[k] == sb[k]).all()
+    assert torch.equal(a.device_kv[0][: R * (H + S * K)], b.device_kv[0][: R * (H + S * K)])
+    assert a.status() == (0, 0) and b.status() == (0, 0)
