@@ -16,9 +16,10 @@
 //      - admitted misses: all if U <= cap, otherwise the m best by (last step
 //        descending, ordinal ascending);
 //      - the i-th admitted miss (ascending ordinal) takes the i-th victim
-//        (ascending slot): its old token leaves the hash, phys[v] and
-//        phys[H + j] swap (the copied row becomes the hot row, no second
-//        copy), the new token enters the hash and the slot takes epoch E.
+//        (ascending slot): its old token leaves the token -> slot index
+//        (hash bank or dense map), phys[v] and phys[H + j] swap (the copied
+//        row becomes the hot row, no second copy), the new token enters the
+//        index and the slot takes epoch E.
 //  * the other CTAs copy every unique miss's KV row from the mapped pinned
 //    host pool to the device row the gather returned for it: 16-byte
 //    vectors, consecutive threads on consecutive 16-byte pieces of a row,

@@ -11,8 +11,9 @@
 //   3. write the ascending page list (padded with -1) and, per entry,
 //      rank * page_size + t % page_size.
 //
-// Reset: returns (layer, request) states to empty: hash bank unused, epochs
-// and tokens -1, position table the identity, control words zero.
+// Reset: returns (layer, request) states to empty: hash bank unused or dense
+// map all -1, epochs and tokens -1, position table the identity, control
+// words zero.
 #include "hs_internal.cuh"
 
 namespace hs {
