@@ -44,8 +44,8 @@ METRIC = "selected tokens resolved/s per layer-call"
 #   reads, 32 B sectors) and dram__bytes_read + write; gather_kernel: DRAM bytes.
 # Other workloads have no capture, so their traffic is reported as null.
 NCU_TRAFFIC = {("C2", "dense"): {"commit_copy_host_link_bytes": 348905 * 32,
-                                 "commit_copy_dram_bytes": 3906645 + 25088,
-                                 "gather_dram_bytes": 5014187},
+                                 "commit_copy_dram_bytes": 3965696 + 26880,
+                                 "gather_dram_bytes": 5014101},
                ("C2", "hash"): {"commit_copy_host_link_bytes": 347942 * 32,
                                 "commit_copy_dram_bytes": 8077312 + 2560,
                                 "gather_dram_bytes": 5837568}}

@@ -255,6 +255,15 @@ int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t
  * set, HS_OK otherwise. */
 int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream);
 
+/* Running sums of the per-request counters (HS_STAT_*) of layer `layer_id`
+ * over every swap-in call since the handle was created or last read with
+ * `reset` (a monitoring aid: hit rate, misses, evictions, overflow).  Rows
+ * rejected on the device add nothing.  Copies HS_NUM_STATS int64 values to
+ * totals_host (indexed by HS_STAT_*) and synchronises `stream`; reset != 0
+ * then sets the sums to zero (ordered on `stream`). */
+int hs_get_stats(hs_state* st, int32_t layer_id, int64_t* totals_host, int32_t reset,
+                 void* stream);
+
 /* Copies one request's policy state of one layer to host memory and
  * synchronises `stream` (checkpointing and tests).  Any output may be NULL.
  *   tok_host  int32 [H]: token held by each hot slot, -1 if empty

@@ -96,6 +96,7 @@ def _declare(lib) -> None:
                                          _vp]),
         "hs_reset_requests": (ctypes.c_int, [_vp, _vp, _i32, _vp]),
         "hs_get_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+        "hs_get_stats": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp]),
         "hs_export_request_state": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
                                                    _vp]),
         "hs_swap_in_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
@@ -325,6 +326,16 @@ def hs_append_rows(handle: StateHandle, layer_id: int, req, tok, seq_lens, rows,
         _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(rows, torch.uint8, "rows"), n,
         _stream_ptr(stream))
     _check(rc, "hs_append_rows")
+
+
+def hs_get_stats(handle: StateHandle, layer_id: int, reset: bool = False, stream=None):
+    """Running sums of the HS_STAT_* counters of one layer: int64 [HS_NUM_STATS]."""
+    import numpy as np
+    out = np.zeros(HS_NUM_STATS, dtype=np.int64)
+    rc = load_library().hs_get_stats(handle.ptr, layer_id, out.ctypes.data, 1 if reset else 0,
+                                     _stream_ptr(stream))
+    _check(rc, "hs_get_stats")
+    return out
 
 
 def hs_set_phase_event(handle: StateHandle, event=None) -> None:

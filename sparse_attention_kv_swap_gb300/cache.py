@@ -73,6 +73,10 @@ class SwapInCache:
     def reset_requests(self, req_pool_indices: torch.Tensor, stream=None) -> None:
         B.hs_reset_requests(self.handle, req_pool_indices, stream)
 
+    def totals(self, layer_id: int = 0, reset: bool = False, stream=None):
+        """Running sums of the per-request counters of one layer (HS_STAT_* order)."""
+        return B.hs_get_stats(self.handle, layer_id, reset, stream)
+
     def status(self, stream=None):
         return B.hs_get_status(self.handle, stream)
 

@@ -53,6 +53,8 @@ StateLayout state_layout(const Dims& d) {
     o = align256(o + lr * (size_t)(d.H + d.C) * 4);
     s.ctrl = o;
     o = align256(o + lr * kCtrlWords * 4);
+    s.totals = o;
+    o = align256(o + (size_t)d.layers * kTotalsWords * 8);
     s.total = o;
     return s;
 }
@@ -90,6 +92,8 @@ LayerView layer_view(const Dims& d, uint8_t* state, int layer, const uint8_t* ho
     v.tok = reinterpret_cast<int32_t*>(state + s.tok) + lq * d.H;
     v.phys = reinterpret_cast<int32_t*>(state + s.phys) + lq * (d.H + d.C);
     v.ctrl = reinterpret_cast<int32_t*>(state + s.ctrl) + lq * kCtrlWords;
+    v.totals = reinterpret_cast<unsigned long long*>(state + s.totals) +
+               (size_t)layer * kTotalsWords;
     v.host_pool = host_pool;
     v.device_kv = device_kv;
     return v;
@@ -230,6 +234,8 @@ int hs_create_state(const hs_config* cfg, void* const* host_pool_host, void* con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(st->ws + wl.status, 0, 4, s) != cudaSuccess ||
         cudaMemsetAsync(st->ws + wl.cnt, 0, (size_t)d.B_max * kCntWords * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(st->state + sl.totals, 0, (size_t)d.layers * kTotalsWords * 8, s) !=
+            cudaSuccess ||
         launch_reset(d, st->state, nullptr, d.R, s) != cudaSuccess) {
         delete st;
         return HS_ERR_CUDA;
@@ -382,6 +388,21 @@ int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream) {
     if (cudaMemsetAsync(st->ws + st->wl.status, 0, 4, s) != cudaSuccess) return HS_ERR_CUDA;
     *flags_out = flags;
     return flags ? HS_ERR_DEVICE_STATUS : HS_OK;
+}
+
+int hs_get_stats(hs_state* st, int32_t layer_id, int64_t* totals_host, int32_t reset,
+                 void* stream) {
+    if (!st || !totals_host) return HS_ERR_INVALID_ARG;
+    if (layer_id < 0 || layer_id >= st->d.layers) return HS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char* src = st->state + st->sl.totals + (size_t)layer_id * kTotalsWords * 8;
+    unsigned long long buf[HS_NUM_STATS];
+    if (cudaMemcpyAsync(buf, src, sizeof(buf), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return HS_ERR_CUDA;
+    if (reset && cudaMemsetAsync(src, 0, sizeof(buf), s) != cudaSuccess) return HS_ERR_CUDA;
+    for (int k = 0; k < HS_NUM_STATS; ++k) totals_host[k] = (int64_t)buf[k];
+    return HS_OK;
 }
 
 int hs_export_request_state(hs_state* st, int32_t layer_id, int32_t request, int32_t* tok_host,

@@ -362,6 +362,11 @@ __device__ void commit_request(const SwapArgs& a, int b, unsigned* keys) {
             st[HS_STAT_EVICTED] = evicted;
             st[HS_STAT_OVERFLOW] = U - m;
         }
+        unsigned long long* tot = a.lv.totals;  // the layer's running sums
+        atomicAdd(tot + HS_STAT_HIT_SLOTS, (unsigned long long)nhit);
+        atomicAdd(tot + HS_STAT_ADMITTED, (unsigned long long)m);
+        atomicAdd(tot + HS_STAT_EVICTED, (unsigned long long)evicted);
+        atomicAdd(tot + HS_STAT_OVERFLOW, (unsigned long long)(U - m));
     }
 }
 

@@ -350,6 +350,12 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
             st[HS_STAT_INVALID] = n_inv;
             st[HS_STAT_EXTRA] = s_cnt[3];
         }
+        unsigned long long* tot = a.lv.totals;  // the layer's running sums
+        atomicAdd(tot + HS_STAT_HITS, (unsigned long long)n_hit);
+        atomicAdd(tot + HS_STAT_DUP_MISSES, (unsigned long long)(n_miss - U));
+        atomicAdd(tot + HS_STAT_UNIQUE_MISSES, (unsigned long long)U);
+        atomicAdd(tot + HS_STAT_INVALID, (unsigned long long)n_inv);
+        atomicAdd(tot + HS_STAT_EXTRA, (unsigned long long)s_cnt[3]);
         if (a.plan_count) a.plan_count[b] = U;
     }
 }

@@ -10,6 +10,7 @@
 //     tok   int32 [layers][R][H]          token held by the slot (-1 empty)
 //     phys  int32 [layers][R][H + C]      physical row of each position
 //     ctrl  int32 [layers][R][8]          control words (see Ctrl)
+//     totals uint64 [layers][16]          running sums of the HS_STAT_* counters
 //   workspace (one call at a time, shared by all layers):
 //     miss_tok / miss_last / miss_dst / vict / adm  int32 [B_max][C]
 //     cnt   int32 [B_max][16]             per-request call counters
@@ -35,6 +36,7 @@ enum Ctrl : int {
     CTRL_REBUILDS = 4,  // hash rebuilds so far (diagnostic)
 };
 
+constexpr int kTotalsWords = 16;  // per layer; the first HS_NUM_STATS are used
 constexpr int kCntWords = 16;
 enum Cnt : int {
     CNT_U = 0,        // unique misses
@@ -60,6 +62,7 @@ struct LayerView {
     int32_t* tok;              // [R][H]
     int32_t* phys;             // [R][H + C]
     int32_t* ctrl;             // [R][kCtrlWords]
+    unsigned long long* totals;  // [kTotalsWords] running sums of the HS_STAT_* counters
     const uint8_t* host_pool;  // device mapping of the pinned pool [R][L][W]
     uint8_t* device_kv;        // [R * (H + C) + R * E][W]: hot + scratch rows, extra pages
 };
@@ -93,7 +96,7 @@ struct SwapArgs {
 
 // Byte offsets of the state and workspace regions (256-byte aligned).
 struct StateLayout {
-    size_t bank, map, ep, tok, phys, ctrl, total;
+    size_t bank, map, ep, tok, phys, ctrl, totals, total;
 };
 struct WorkspaceLayout {
     size_t miss_tok, miss_last, miss_dst, vict, adm, cnt, status, total;

@@ -158,6 +158,12 @@ def test_extra_page_config(lib):
                                     extra_page_size=1)) == B.HS_ERR_UNSUPPORTED
 
 
+def test_get_stats_argument_errors(lib):
+    import numpy as np
+    out = np.zeros(B.HS_NUM_STATS, np.int64)
+    assert lib.hs_get_stats(None, 0, out.ctypes.data, 0, None) == B.HS_ERR_INVALID_ARG
+
+
 def test_append_rows_argument_errors(lib):
     """hs_append_rows rejects bad handles, layers, counts and unaligned rows on the host."""
     assert lib.hs_append_rows(None, 0, None, None, None, None, 1, None) == B.HS_ERR_INVALID_ARG

@@ -175,3 +175,24 @@ def test_pinned_host_inputs_and_outputs_match_device_buffers():
             for k in ("tok", "ep", "phys"):
                 assert (sa[k] == sb[k]).all()
     assert (a.cache.device_kv[0].cpu() == b.cache.device_kv[0].cpu()).all()
+
+
+def test_running_totals_are_the_sums_of_the_call_counters():
+    """hs_get_stats: per layer, the sum of every call's per-request counters
+    (summed on the oracle side), and reset clears them."""
+    rng = np.random.default_rng(41)
+    run = ParityRun(5, 2000, W.ROW_BYTES, 64, 256, 3, layers=2, extra_page=16, own_pool=True)
+    want = [np.zeros(B.HS_NUM_STATS, np.int64) for _ in range(2)]
+    for c in range(8):
+        layer = c % 2
+        S = int(rng.integers(1, 4))
+        topk = rng.integers(-3, 2000, size=(4, S, 256)).astype(np.int32)
+        rpi = rng.permutation(5)[:4].astype(np.int32)
+        sl = rng.integers(1500, 2001, size=4).astype(np.int32)
+        g = run.call(topk, rpi, sl, layer=layer)
+        want[layer] += g["stats"].sum(axis=0)
+    for layer in range(2):
+        got = run.cache.totals(layer)
+        assert (got == want[layer]).all(), (layer, got, want[layer])
+    assert run.cache.totals(0, reset=True).sum() > 0
+    assert (run.cache.totals(0) == 0).all() and (run.cache.totals(1) == want[1]).all()
