@@ -38,17 +38,23 @@ if ROOT not in sys.path:
 import hs_workloads as W  # noqa: E402
 
 METRIC = "selected tokens resolved/s per layer-call"
-# Per-launch counters of the current kernels on the C2 workload, from one ncu
-# capture of the timed steps (steady state, after an L2 flush), per index:
+# Per-launch counters of the current kernels, from ncu captures of the timed
+# steps (steady state, after an L2 flush), per workload and index:
 #   commit_copy_kernel: syslts__t_sectors_aperture_sysmem_op_read (host-link
 #   reads, 32 B sectors) and dram__bytes_read + write; gather_kernel: DRAM bytes.
-# Other workloads have no capture, so their traffic is reported as null.
+# Combinations without a capture report their traffic as null.
 NCU_TRAFFIC = {("C2", "dense"): {"commit_copy_host_link_bytes": 348905 * 32,
                                  "commit_copy_dram_bytes": 3965696 + 26880,
                                  "gather_dram_bytes": 5014101},
-               ("C2", "hash"): {"commit_copy_host_link_bytes": 347942 * 32,
-                                "commit_copy_dram_bytes": 8077312 + 2560,
-                                "gather_dram_bytes": 5837568}}
+               ("C3", "dense"): {"commit_copy_host_link_bytes": 1299617 * 32,
+                                 "commit_copy_dram_bytes": 9947562 + 2838528,
+                                 "gather_dram_bytes": 8358229},
+               ("C4", "dense"): {"commit_copy_host_link_bytes": 689289 * 32,
+                                 "commit_copy_dram_bytes": 934485 + 16469,
+                                 "gather_dram_bytes": 1382485},
+               ("C5", "dense"): {"commit_copy_host_link_bytes": 53057 * 32,
+                                 "commit_copy_dram_bytes": 1794048 + 170,
+                                 "gather_dram_bytes": 1046101}}
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
 # Untimed steps run right after each gate, before the timed ones.  On GB300
