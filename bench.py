@@ -60,9 +60,10 @@ PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in s
 # Untimed steps run right after each gate, before the timed ones.  On GB300
 # the first step after the gate always ran about twice as slow as the rest,
 # and about one run in five began with a slow stretch of up to ~15 ms (steps
-# up to 10x slow, decaying), host enqueue well ahead of the GPU throughout;
-# 16 primer steps (2.5 ms of C2 work) absorbed it in every run we made.
-PRIMER_STEPS = 16
+# up to 10x slow, decaying), host enqueue well ahead of the GPU throughout.
+# 16 primer steps (2.5 ms of C2 work) absorbed most of it; 64 (10 ms of C2
+# work, 20 ms of C3) leave the timed steps clear of the longest stretches seen.
+PRIMER_STEPS = 64
 FLUSH_BYTES = 256 << 20
 
 
