@@ -101,20 +101,6 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
     unsigned xbits = 0u;  // bit r: entry r is on the extra page
     const long long base = (long long)q * (d.H + d.C);
     const int32_t* phys = a.lv.phys + base;
-    if (q_ok) {
-        // Warm L2 with this CTA's share of the request's position table and
-        // token -> slot index: the probes and position loads below find them.
-        const size_t stride = (size_t)P * BD * 128, off0 = ((size_t)c * BD + tid) * 128;
-        const char* prow = reinterpret_cast<const char*>(phys);
-        for (size_t off = off0; off < (size_t)(d.H + d.C) * 4; off += stride)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(prow + off));
-        const char* irow = d.dense
-            ? reinterpret_cast<const char*>(a.lv.map + (long long)q * d.L)
-            : reinterpret_cast<const char*>(a.lv.bank + (long long)q * d.hash_size);
-        const size_t ibytes = d.dense ? (size_t)d.L * 2 : (size_t)d.hash_size * 8;
-        for (size_t off = off0; off < ibytes; off += stride)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(irow + off));
-    }
     for (int i = tid; i < TS; i += BD) {
         keys[i] = -1;
         first[i] = 0x7fffffff;
