@@ -162,13 +162,51 @@ def _stream_ptr(stream) -> int:
 
 
 def _dptr(t, dtype=None, name="tensor") -> int:
+    """Address of a tensor the kernels read or write: device memory, or pinned
+    (mapped) host memory, which the device addresses directly."""
     if t is None:
         return 0
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
         raise ValueError("%s must have dtype %s" % (name, dtype))
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("%s must be in device memory or pinned host memory" % name)
     return int(t.data_ptr())
+
+
+def _hptr(t, name="tensor") -> int:
+    """Address of a host pool: pinned, or pageable where the library accepts it
+    (it checks the memory kind itself)."""
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return int(t.data_ptr())
+
+
+def _shape(t, shape, name) -> None:
+    """The kernels trust the sizes: check them before any launch."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _swap_in_shapes(handle, req_pool_indices, seq_lens, topk, device_locs, stats, miss_src,
+                    miss_dst, miss_count):
+    if topk.dim() != 3:
+        raise ValueError("topk must be [batch, steps, top_k]")
+    B, S, K = topk.shape
+    cfg = handle.cfg
+    if K != cfg.top_k:
+        raise ValueError("topk's last dimension %d differs from the config's top_k %d"
+                         % (K, cfg.top_k))
+    C = cfg.max_steps * cfg.top_k
+    _shape(req_pool_indices, (B,), "req_pool_indices")
+    _shape(seq_lens, (B,), "seq_lens")
+    _shape(device_locs, (B, S, K), "device_locs")
+    _shape(stats, (B, HS_NUM_STATS), "stats")
+    _shape(miss_src, (B, C), "miss_src")
+    _shape(miss_dst, (B, C), "miss_dst")
+    _shape(miss_count, (B,), "miss_count")
+    return B, S, K
 
 
 # ---- sizes -----------------------------------------------------------------
@@ -233,7 +271,7 @@ def hs_create_state(cfg: HsConfig, host_pools: Sequence, device_kvs: Sequence, s
     L = cfg.num_layers
     if len(host_pools) != L or len(device_kvs) != L:
         raise ValueError("need one host pool and one device KV buffer per layer")
-    hp = (ctypes.c_void_p * L)(*[_dptr(t, name="host pool") for t in host_pools])
+    hp = (ctypes.c_void_p * L)(*[_hptr(t, name="host pool") for t in host_pools])
     dk = (ctypes.c_void_p * L)(*[_dptr(t, name="device kv") for t in device_kvs])
     out = ctypes.c_void_p()
     rc = lib.hs_create_state(ctypes.byref(cfg), ctypes.cast(hp, _vp), ctypes.cast(dk, _vp),
@@ -253,7 +291,8 @@ def hs_swap_in(handle: StateHandle, req_pool_indices, seq_lens, topk, layer_id: 
                device_locs, stats=None, miss_src=None, miss_dst=None, miss_count=None,
                stream=None) -> None:
     import torch
-    B, S, K = topk.shape
+    B, S, K = _swap_in_shapes(handle, req_pool_indices, seq_lens, topk, device_locs, stats,
+                              miss_src, miss_dst, miss_count)
     rc = load_library().hs_swap_in(
         handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
         _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
@@ -267,7 +306,13 @@ def hs_swap_in(handle: StateHandle, req_pool_indices, seq_lens, topk, layer_id: 
 def hs_page_table(topk, seq_lens, max_seq_len: int, page_size: int, pages, num_pages,
                   token_page, stream=None) -> None:
     import torch
+    if topk.dim() != 3:
+        raise ValueError("topk must be [batch, steps, top_k]")
     B, S, K = topk.shape
+    _shape(seq_lens, (B,), "seq_lens")
+    _shape(pages, (B, S * K), "pages")
+    _shape(num_pages, (B,), "num_pages")
+    _shape(token_page, (B, S, K), "token_page")
     rc = load_library().hs_page_table(
         _dptr(topk, torch.int32, "topk"), _dptr(seq_lens, torch.int32, "seq_lens"), B, S, K,
         max_seq_len, page_size, _dptr(pages, torch.int32, "pages"),
@@ -278,6 +323,8 @@ def hs_page_table(topk, seq_lens, max_seq_len: int, page_size: int, pages, num_p
 
 def hs_reset_requests(handle: StateHandle, req_pool_indices, stream=None) -> None:
     import torch
+    if req_pool_indices.dim() != 1:
+        raise ValueError("req_pool_indices must be 1-D")
     rc = load_library().hs_reset_requests(
         handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
         req_pool_indices.numel(), _stream_ptr(stream))
@@ -319,8 +366,10 @@ def hs_append_rows(handle: StateHandle, layer_id: int, req, tok, seq_lens, rows,
     [n, W] on the device (see the C header)."""
     import torch
     n = req.numel()
-    if tok.numel() != n or seq_lens.numel() != n or rows.dim() != 2 or rows.shape[0] != n:
-        raise ValueError("req, tok, seq_lens and rows must describe the same n entries")
+    _shape(req, (n,), "req")
+    _shape(tok, (n,), "tok")
+    _shape(seq_lens, (n,), "seq_lens")
+    _shape(rows, (n, handle.cfg.item_size_bytes), "rows")
     rc = load_library().hs_append_rows(
         handle.ptr, layer_id, _dptr(req, torch.int32, "req"), _dptr(tok, torch.int32, "tok"),
         _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(rows, torch.uint8, "rows"), n,
@@ -355,6 +404,11 @@ def hs_set_defer_copy(handle: StateHandle, defer: bool) -> None:
 def hs_copy_planned(handle: StateHandle, layer_id: int, miss_src, miss_dst, miss_count,
                     stream=None) -> None:
     import torch
+    B = miss_count.numel()
+    C = handle.cfg.max_steps * handle.cfg.top_k
+    _shape(miss_count, (B,), "miss_count")
+    _shape(miss_src, (B, C), "miss_src")
+    _shape(miss_dst, (B, C), "miss_dst")
     rc = load_library().hs_copy_planned(
         handle.ptr, layer_id, _dptr(miss_src, torch.int64, "miss_src"),
         _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
@@ -368,7 +422,8 @@ def hs_swap_in_noalloc(handle: StateHandle, req_pool_indices, seq_lens, topk, la
     """hs_swap_in whose per-call scratch is the library's fixed device array
     (for callers that cannot allocate device memory); see the C header."""
     import torch
-    B, S, K = topk.shape
+    B, S, K = _swap_in_shapes(handle, req_pool_indices, seq_lens, topk, device_locs, stats,
+                              miss_src, miss_dst, miss_count)
     rc = load_library().hs_swap_in_noalloc(
         handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
         _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,

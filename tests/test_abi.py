@@ -167,3 +167,40 @@ def test_get_stats_argument_errors(lib):
 def test_append_rows_argument_errors(lib):
     """hs_append_rows rejects bad handles, layers, counts and unaligned rows on the host."""
     assert lib.hs_append_rows(None, 0, None, None, None, None, 1, None) == B.HS_ERR_INVALID_ARG
+
+
+def test_binding_checks_shapes_and_memory_before_any_launch():
+    """The kernels trust the sizes they are given: the binding rejects wrong
+    shapes, top-k widths and unpinned host tensors before calling the library."""
+    import torch
+
+    class Handle:  # never reaches the library: every call below fails first
+        ptr = None
+        cfg = _cfg(num_requests=8, max_seq_len=100, hot_buffer_size=16, top_k=4, max_steps=2,
+                   max_batch=8)
+
+    # plain host tensors: the shape checks come before the memory check, which
+    # then rejects them (they are neither device nor pinned memory)
+    i32 = dict(dtype=torch.int32)
+    h = Handle()
+    topk = torch.zeros((2, 1, 4), **i32)
+    rpi = torch.zeros(2, **i32)
+    locs = torch.zeros((2, 1, 4), **i32)
+    with pytest.raises(ValueError, match="top_k"):
+        B.hs_swap_in(h, rpi, rpi, torch.zeros((2, 1, 5), **i32), 0, locs)
+    with pytest.raises(ValueError, match="seq_lens"):
+        B.hs_swap_in(h, rpi, torch.zeros(3, **i32), topk, 0, locs)
+    with pytest.raises(ValueError, match="device_locs"):
+        B.hs_swap_in(h, rpi, rpi, topk, 0, torch.zeros((2, 2, 4), **i32))
+    with pytest.raises(ValueError, match="stats"):
+        B.hs_swap_in(h, rpi, rpi, topk, 0, locs, torch.zeros((2, 8), **i32))
+    with pytest.raises(ValueError, match="miss_src"):
+        B.hs_swap_in(h, rpi, rpi, topk, 0, locs, None, torch.zeros((2, 4), dtype=torch.int64),
+                     torch.zeros((2, 8), dtype=torch.int64), rpi)
+    with pytest.raises(ValueError, match="pinned"):
+        B.hs_swap_in(h, rpi, rpi, topk, 0, locs)
+    with pytest.raises(ValueError, match="rows"):
+        B.hs_append_rows(h, 0, rpi, rpi, rpi, torch.zeros((2, 64), dtype=torch.uint8))
+    with pytest.raises(ValueError, match="token_page"):
+        B.hs_page_table(topk, rpi, 100, 16, torch.zeros((2, 4), **i32), rpi,
+                        torch.zeros((2, 4), **i32))
