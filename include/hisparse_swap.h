@@ -73,6 +73,7 @@ extern "C" {
 #define HS_STATUS_PROBE_LIMIT 0x8u       /* hash probe exceeded the table      */
 #define HS_STATUS_TABLE_FULL 0x10u       /* hash insert found no free entry    */
 #define HS_STATUS_BAD_APPEND 0x20u       /* hs_append_rows entry out of range  */
+#define HS_STATUS_BAD_PLAN 0x40u         /* hs_copy_planned row/count out of range */
 
 /* ---- per-request counters of one call (int32 [B, HS_NUM_STATS]) -------- */
 #define HS_STAT_HITS 0          /* valid entries whose token was resident   */
@@ -293,7 +294,9 @@ int hs_set_defer_copy(hs_state* st, int32_t defer);
  * miss_count[b], host row miss_src[b, j] of layer `layer_id`'s pool to
  * device row miss_dst[b, j] of its device buffer (W bytes each).  The plan
  * is exactly what hs_swap_in wrote ([batch, C] with C = max_steps * top_k).
- * Asynchronous on `stream`. */
+ * A count outside [0, C] is clamped and a row outside the pool or the
+ * device buffer is skipped; either sets HS_STATUS_BAD_PLAN.  Asynchronous on
+ * `stream`. */
 int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
                     const int64_t* miss_dst_dev, const int32_t* miss_count_dev, int32_t batch,
                     void* stream);

@@ -31,6 +31,7 @@ HS_STATUS_SEQ_LEN_CLAMPED = 0x4
 HS_STATUS_PROBE_LIMIT = 0x8
 HS_STATUS_TABLE_FULL = 0x10
 HS_STATUS_BAD_APPEND = 0x20
+HS_STATUS_BAD_PLAN = 0x40
 
 HS_INDEX_HASH = 0
 HS_INDEX_DENSE = 1

@@ -328,7 +328,9 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
     return launch_planned_copy(reinterpret_cast<const long long*>(miss_src_dev),
                                reinterpret_cast<const long long*>(miss_dst_dev), miss_count_dev,
                                batch, d.C, d.W, st->host_pool_dev[layer_id],
-                               st->device_kv[layer_id], st->copy_ctas,
+                               (long long)d.R * d.L, st->device_kv[layer_id],
+                               (long long)d.R * (d.H + d.C + d.E),
+                               reinterpret_cast<uint32_t*>(st->ws + st->wl.status), st->copy_ctas,
                                static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HS_OK
                : HS_ERR_CUDA;

@@ -383,6 +383,7 @@ struct WorkspaceRows {
         *src = (long long)cnt[(long long)b * kCntWords + CNT_Q] * L + miss_tok[wi];
         *dst = miss_dst[wi];
     }
+    __device__ bool valid(long long, long long) const { return true; }  // written by the gather
 };
 
 // ... or a recorded miss plan (host row, device row, count per batch row).
@@ -391,10 +392,24 @@ struct RecordedRows {
     const long long* dst;
     const int32_t* count_;
     int32_t C;
-    __device__ int count(int b) const { return count_[b]; }
+    long long src_rows, dst_rows;  // rows of the host pool and of the device buffer
+    uint32_t* status;
+    // The plan comes from the caller: a count outside [0, C] is clamped and a
+    // row outside its buffer is skipped, both flagged, never accessed.
+    __device__ int count(int b) const {
+        const int n = count_[b];
+        if (n >= 0 && n <= C) return n;
+        atomicOr(status, HS_STATUS_BAD_PLAN);
+        return n < 0 ? 0 : C;
+    }
     __device__ void rows(int b, int j, long long* s, long long* d) const {
         *s = src[(long long)b * C + j];
         *d = dst[(long long)b * C + j];
+    }
+    __device__ bool valid(long long s, long long d) const {
+        if (s >= 0 && s < src_rows && d >= 0 && d < dst_rows) return true;
+        atomicOr(status, HS_STATUS_BAD_PLAN);
+        return false;
     }
 };
 
@@ -445,8 +460,10 @@ __device__ void copy_rows(const Rows& plan, int B, int W, const uint8_t* pool, u
                 }
                 long long srow, drow;
                 plan.rows(lo, row - pre[lo], &srow, &drow);
-                dst[u] = drow * W + ((long long)piece << 4);
-                v[u] = ld_stream_v4(pool + srow * W + ((long long)piece << 4));
+                if (plan.valid(srow, drow)) {
+                    dst[u] = drow * W + ((long long)piece << 4);
+                    v[u] = ld_stream_v4(pool + srow * W + ((long long)piece << 4));
+                }
             }
         }
 #pragma unroll
@@ -515,12 +532,13 @@ cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaS
 
 cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
                                 int32_t B, int32_t C, int32_t W, const uint8_t* pool,
-                                uint8_t* kv, int ctas, cudaStream_t s) {
+                                long long pool_rows, uint8_t* kv, long long kv_rows,
+                                uint32_t* status, int ctas, cudaStream_t s) {
     static int cached = 48 * 1024;
     const size_t smem = (size_t)(B + 1) * 4;
     cudaError_t e = ensure_smem(planned_copy_kernel, smem, &cached);
     if (e != cudaSuccess) return e;
-    const RecordedRows plan{src, dst, count, C};
+    const RecordedRows plan{src, dst, count, C, pool_rows, kv_rows, status};
     planned_copy_kernel<<<ctas, kBlock, smem, s>>>(plan, B, W, pool, kv);
     return cudaGetLastError();
 }

@@ -127,7 +127,8 @@ size_t commit_smem_bytes(const Dims& d);
 cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s);
 cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
                                 int32_t B, int32_t C, int32_t W, const uint8_t* pool,
-                                uint8_t* kv, int ctas, cudaStream_t s);
+                                long long pool_rows, uint8_t* kv, long long kv_rows,
+                                uint32_t* status, int ctas, cudaStream_t s);
 cudaError_t launch_append(const Dims& d, const LayerView& lv, uint8_t* host_pool,
                           const int32_t* req, const int32_t* tok, const int32_t* seq_lens,
                           const uint8_t* rows, int32_t n, uint32_t* status, cudaStream_t s);

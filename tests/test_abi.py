@@ -30,7 +30,7 @@ def test_header_constants_match_binding():
                  "HS_ERR_DEVICE_STATUS", "HS_ERR_TIMEOUT", "HS_STATUS_BAD_REQUEST",
                  "HS_STATUS_DUPLICATE_REQUEST", "HS_STATUS_SEQ_LEN_CLAMPED",
                  "HS_STATUS_PROBE_LIMIT", "HS_STATUS_TABLE_FULL", "HS_STATUS_BAD_APPEND",
-                 "HS_NUM_STATS", "HS_MAX_EXTRA_PAGE", "HS_STAT_EXTRA"):
+                 "HS_NUM_STATS", "HS_MAX_EXTRA_PAGE", "HS_STAT_EXTRA", "HS_STATUS_BAD_PLAN"):
         assert int(consts[name], 0) == getattr(B, name), name
 
 

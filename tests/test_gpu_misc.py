@@ -196,3 +196,36 @@ def test_running_totals_are_the_sums_of_the_call_counters():
         assert (got == want[layer]).all(), (layer, got, want[layer])
     assert run.cache.totals(0, reset=True).sum() > 0
     assert (run.cache.totals(0) == 0).all() and (run.cache.totals(1) == want[1]).all()
+
+
+def test_planned_copy_skips_out_of_range_plans():
+    """hs_copy_planned takes the caller's plan: out-of-range rows are skipped
+    and counts are clamped to [0, C], with HS_STATUS_BAD_PLAN set; the valid
+    rows are still copied."""
+    R, L, Wd, H, K, S = 3, 50, 32, 4, 4, 1
+    C = S * K
+    run = ParityRun(R, L, Wd, H, K, S)
+    kv = run.cache.device_kv[0]
+    rows_total = kv.shape[0]
+    src = np.zeros((3, C), np.int64)
+    dst = np.zeros((3, C), np.int64)
+    cnt = np.array([3, C + 5, -2], np.int32)   # row 1 clamps to C, row 2 to 0
+    src[0, :3] = [0 * L + 7, R * L, 2 * L + 9]   # the middle source is past the pool
+    dst[0, :3] = [0, 1, -1]                      # the last destination is negative
+    src[1, :] = 1 * L + np.arange(C)
+    dst[1, :] = (H + C) + H + np.arange(C)
+    d = lambda a: torch.from_numpy(a).cuda()
+    kv.zero_()
+    pkg.hs_copy_planned(run.cache.handle, 0, d(src), d(dst), d(cnt))
+    torch.cuda.synchronize()
+    rc, flags = run.cache.status()
+    assert flags == B.HS_STATUS_BAD_PLAN
+    got = kv.cpu().numpy()
+    pool = run.pools[0].numpy()
+    assert (got[0] == pool[0, 7]).all()                 # the one valid row of batch row 0
+    assert (got[1] == 0).all()                          # its invalid rows wrote nothing
+    for j in range(C):                                  # batch row 1: clamped to C rows
+        assert (got[(H + C) + H + j] == pool[1, j]).all()
+    untouched = np.ones(rows_total, bool)
+    untouched[[0] + [(H + C) + H + j for j in range(C)]] = False
+    assert (got[untouched] == 0).all()
