@@ -5,7 +5,10 @@
  * indexer top-k token indices against a per-request device hot buffer that
  * is backed by a pinned host KV pool, and returns the device row of every
  * selected token (plus, on request, a sparse page table).  One call:
- *   1. looks each token up in the request's token -> slot hash,
+ *   0. serves tokens on the request's extra page (its newest, still-filling
+ *      page, when configured) without a lookup,
+ *   1. looks the others up in the request's token -> slot index (hash bank
+ *      or dense map),
  *   2. de-duplicates misses within and across the speculative steps,
  *   3. copies each unique miss's KV row from mapped pinned host memory into a
  *      scratch row of the device buffer,
@@ -25,7 +28,9 @@
  *    read or write it across the host link, e.g. NVLink-C2C on Grace.
  *    The caller owns every buffer (pinned host pool, device KV buffers,
  *    state, workspace, inputs, outputs).  The library owns only the small
- *    host handle `hs_state`.
+ *    host handle `hs_state`.  Buffer sizes follow from the config and the
+ *    call's arguments as each function states; the kernels trust them (the
+ *    Python binding checks tensor shapes before calling).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are asynchronous on that stream unless stated.  Calls
  *    that share one hs_state must be ordered on one stream (or by events):
