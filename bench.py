@@ -393,7 +393,7 @@ def decode_step_extra_page(torch, pkg, w, dev, flush, calls, pool, dense, E=256,
 
 
 def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers=4, n=10,
-                           copy_ctas=0):
+                           copy_ctas=32):
     """F2 in use: a `layers`-layer decode step, swap-in after swap-in on one
     stream, against the deferred-copy protocol, where each layer's swap-in only
     resolves and commits and its recorded miss plan is copied on a second
@@ -421,7 +421,8 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
              for l in range(layers)]
     s0 = torch.cuda.current_stream()
     # two copy streams, alternating by layer, so that one layer's copy can
-    # start while the previous one drains
+    # start while the previous one drains; 32 CTAs per copy keep the link full
+    # and leave the SMs that the next layer's gather needs
     copy_streams = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
     done = [torch.cuda.Event() for _ in range(layers)]
 
