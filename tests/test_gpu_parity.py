@@ -186,17 +186,17 @@ def test_workload_full_size_dense_index(name):
                  properties=(name == "C4" and c == 5))
 
 
-@pytest.mark.parametrize("name", ["C2", "C3"])
-def test_full_size_graph_replay_as_benchmarked(name):
-    """The benchmark's launch configuration at full size: dense index, one
-    swap-in captured in a CUDA graph on a side stream and replayed with each
-    call's top-k staged into the graph's input buffer."""
+@pytest.mark.parametrize("name,dense", [("C2", True), ("C3", True), ("C2", False)])
+def test_full_size_graph_replay_as_benchmarked(name, dense):
+    """The benchmark's launch configuration at full size (dense index, and the
+    hash banks as well): one swap-in captured in a CUDA graph on a side stream
+    and replayed with each call's top-k staged into the graph's input buffer."""
     import torch
     import sparse_attention_kv_swap_gb300 as pkg
     w = W.WORKLOADS[name]
     stream = W.TopkStream(w)
     rpi, sl = W.req_pool_indices(w), W.seq_lens(w)
-    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, dense=True)
+    run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, dense=dense)
     run.call(stream.next_call(), rpi, sl, compare_rows=False)  # also sets kernel attributes
     dev = torch.device("cuda")
     rpi_t, sl_t = torch.from_numpy(rpi).to(dev), torch.from_numpy(sl).to(dev)
