@@ -34,7 +34,13 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are asynchronous on that stream unless stated.  Calls
  *    that share one hs_state must be ordered on one stream (or by events):
- *    they share the state and the workspace.
+ *    they share the state and the workspace.  Separate handles are
+ *    independent: their calls may run concurrently from several host
+ *    threads and on several streams.
+ *  - A handle belongs to the device that was current at hs_create_state.
+ *    Every call on it must be made with that device current (and a stream
+ *    of that device); otherwise it returns HS_ERR_INVALID_ARG and launches
+ *    nothing.
  *  - Return value: HS_OK (0) or a negative HS_ERR_* code; nothing aborts or
  *    throws.  Argument errors are detected on the host before any launch.
  *    Data-dependent problems found by the kernels (request index out of

@@ -251,6 +251,7 @@ int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t*
                int32_t* device_locs_dev, int32_t* stats_dev, int64_t* miss_src_dev,
                int64_t* miss_dst_dev, int32_t* miss_count_dev, void* stream) {
     if (!st) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     const Dims& d = st->d;
     if (batch < 0 || batch > d.B_max) return HS_ERR_INVALID_ARG;
     if (num_steps < 1 || num_steps > d.S_max) return HS_ERR_INVALID_ARG;
@@ -292,6 +293,7 @@ int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
                    const int32_t* tok_dev, const int32_t* seq_lens_dev, const void* rows_dev,
                    int32_t n, void* stream) {
     if (!st) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     const Dims& d = st->d;
     if (layer_id < 0 || layer_id >= d.layers || n < 0) return HS_ERR_INVALID_ARG;
     if (n == 0) return HS_OK;
@@ -320,6 +322,7 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
                     const int64_t* miss_dst_dev, const int32_t* miss_count_dev, int32_t batch,
                     void* stream) {
     if (!st) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     const Dims& d = st->d;
     if (layer_id < 0 || layer_id >= d.layers || batch < 0 || batch > d.B_max)
         return HS_ERR_INVALID_ARG;
@@ -371,6 +374,7 @@ int hs_page_table(const int32_t* topk_dev, const int32_t* seq_lens_dev, int32_t 
 int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t n,
                       void* stream) {
     if (!st || n < 0) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     if (n == 0) return HS_OK;
     if (!req_pool_indices_dev || n > st->d.R) return HS_ERR_INVALID_ARG;
     return launch_reset(st->d, st->state, req_pool_indices_dev, n,
@@ -381,6 +385,7 @@ int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t
 
 int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream) {
     if (!st || !flags_out) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t flags = 0;
     if (cudaMemcpyAsync(&flags, st->ws + st->wl.status, 4, cudaMemcpyDeviceToHost, s) !=
@@ -395,6 +400,7 @@ int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream) {
 int hs_get_stats(hs_state* st, int32_t layer_id, int64_t* totals_host, int32_t reset,
                  void* stream) {
     if (!st || !totals_host) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     if (layer_id < 0 || layer_id >= st->d.layers) return HS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned char* src = st->state + st->sl.totals + (size_t)layer_id * kTotalsWords * 8;
@@ -411,6 +417,7 @@ int hs_export_request_state(hs_state* st, int32_t layer_id, int32_t request, int
                             int32_t* ep_host, int32_t* phys_host, int32_t* ctrl_host,
                             int64_t* bank_host, void* stream) {
     if (!st) return HS_ERR_INVALID_ARG;
+    if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     const Dims& d = st->d;
     if (layer_id < 0 || layer_id >= d.layers || request < 0 || request >= d.R)
         return HS_ERR_INVALID_ARG;

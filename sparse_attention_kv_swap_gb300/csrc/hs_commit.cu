@@ -513,9 +513,9 @@ size_t commit_smem_bytes(const Dims& d) {
 }
 
 cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s) {
-    static int cached = 48 * 1024;
+    static SmemOptIn opt_in;
     const size_t smem = commit_smem_bytes(a.d);
-    cudaError_t e = ensure_smem(commit_copy_kernel, smem, &cached);
+    cudaError_t e = ensure_smem(commit_copy_kernel, smem, &opt_in);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.B + copy_ctas);
@@ -534,9 +534,9 @@ cudaError_t launch_planned_copy(const long long* src, const long long* dst, cons
                                 int32_t B, int32_t C, int32_t W, const uint8_t* pool,
                                 long long pool_rows, uint8_t* kv, long long kv_rows,
                                 uint32_t* status, int ctas, cudaStream_t s) {
-    static int cached = 48 * 1024;
+    static SmemOptIn opt_in;
     const size_t smem = (size_t)(B + 1) * 4;
-    cudaError_t e = ensure_smem(planned_copy_kernel, smem, &cached);
+    cudaError_t e = ensure_smem(planned_copy_kernel, smem, &opt_in);
     if (e != cudaSuccess) return e;
     const RecordedRows plan{src, dst, count, C, pool_rows, kv_rows, status};
     planned_copy_kernel<<<ctas, kBlock, smem, s>>>(plan, B, W, pool, kv);

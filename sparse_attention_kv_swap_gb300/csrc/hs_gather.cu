@@ -362,8 +362,8 @@ __global__ void __launch_bounds__(1024, 1) gather_kernel(const SwapArgs a) {
 
 template <int RMAX>
 cudaError_t launch_rmax(const SwapArgs& a, int cluster, int block, size_t smem, cudaStream_t s) {
-    static int cached = 48 * 1024;
-    cudaError_t e = ensure_smem(gather_kernel<RMAX>, smem, &cached);
+    static SmemOptIn opt_in;
+    cudaError_t e = ensure_smem(gather_kernel<RMAX>, smem, &opt_in);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.B * cluster);

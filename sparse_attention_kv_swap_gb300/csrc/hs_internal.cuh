@@ -20,6 +20,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "hisparse_swap.h"
 
 namespace hs {
@@ -108,14 +111,35 @@ LayerView layer_view(const Dims& d, uint8_t* state, int layer, const uint8_t* ho
                      uint8_t* device_kv);
 Workspace workspace_view(const Dims& d, uint8_t* ws);
 
-// Raises a kernel's dynamic shared-memory limit to at least `bytes`
-// (remembered in `*cached`, so repeated calls cost nothing).
+// The dynamic shared-memory size a kernel has been opened up to, per device
+// (cudaFuncSetAttribute acts on the calling thread's current device).  Reads
+// are lock-free; raising the limit takes the mutex, so that concurrent host
+// threads leave the attribute and the remembered size equal.
+struct SmemOptIn {
+    static constexpr int kMaxDevices = 64;
+    std::atomic<int> bytes[kMaxDevices];
+    std::mutex raise;
+    SmemOptIn() {
+        for (auto& b : bytes) b.store(48 * 1024, std::memory_order_relaxed);
+    }
+};
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`; repeated calls cost one atomic load.
 template <typename F>
-cudaError_t ensure_smem(F* kernel, size_t bytes, int* cached) {
-    if ((int)bytes <= *cached) return cudaSuccess;
-    cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e == cudaSuccess) *cached = (int)bytes;
+cudaError_t ensure_smem(F* kernel, size_t bytes, SmemOptIn* opt) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= SmemOptIn::kMaxDevices)
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)bytes);
+    if ((int)bytes <= opt->bytes[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(opt->raise);
+    if ((int)bytes <= opt->bytes[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) opt->bytes[dev].store((int)bytes, std::memory_order_release);
     return e;
 }
 
@@ -224,3 +248,11 @@ struct hs_state {
     cudaEvent_t phase_event;  // profiling split between the two kernels, or null
     int defer_copy;           // 1: hs_swap_in records the miss plan but copies nothing
 };
+
+// True when the calling thread's current device is the one the handle was
+// created on.  Every entry point that launches or copies checks it, so that a
+// call made while another device is current fails instead of running there.
+inline bool on_handle_device(const hs_state* st) {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == st->device;
+}

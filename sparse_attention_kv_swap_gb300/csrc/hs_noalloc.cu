@@ -76,6 +76,7 @@ extern "C" int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_
 
     int device = -1;
     if (cudaGetDevice(&device) != cudaSuccess) return HS_ERR_CUDA;
+    if (device != st->device) return HS_ERR_INVALID_ARG;
     unsigned char* scratch = nullptr;
     if (scratch_address(device, &scratch) != cudaSuccess) return HS_ERR_CUDA;
 

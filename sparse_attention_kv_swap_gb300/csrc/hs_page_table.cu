@@ -112,8 +112,8 @@ cudaError_t launch_page_table(const int32_t* topk, const int32_t* seq_lens, int3
     const long long npages = ((long long)L_max + page_size - 1) / page_size;
     const int nwords = (int)((npages + 31) / 32);
     const size_t smem = (size_t)nwords * 8;
-    static int cached = 48 * 1024;
-    cudaError_t e = ensure_smem(page_table_kernel, smem, &cached);
+    static SmemOptIn opt_in;
+    cudaError_t e = ensure_smem(page_table_kernel, smem, &opt_in);
     if (e != cudaSuccess) return e;
     page_table_kernel<<<B, kPtBlock, smem, s>>>(topk, seq_lens, S, K, L_max, page_size, nwords,
                                                  pages, num_pages, token_page);

@@ -229,3 +229,69 @@ def test_planned_copy_skips_out_of_range_plans():
     untouched = np.ones(rows_total, bool)
     untouched[[0] + [(H + C) + H + j for j in range(C)]] = False
     assert (got[untouched] == 0).all()
+
+
+def test_two_handles_concurrent_threads_and_streams():
+    """Two independent handles (hash index; dense index with an extra page)
+    driven at the same time from two host threads, each on its own stream with
+    no ordering between the streams.  Every call's locations and counters, and
+    each handle's final rows and policy state, equal the oracle's for that
+    handle's own call sequence."""
+    import threading
+    rng = np.random.default_rng(41)
+    specs = [dict(R=6, L=6000, H=400, K=300, S=3, B=6, n=10, dense=False, E=0),
+             dict(R=5, L=3000, H=128, K=200, S=2, B=4, n=12, dense=True, E=64)]
+    runs, calls, ins, outs = [], [], [], []
+    for sp in specs:
+        runs.append(ParityRun(sp["R"], sp["L"], W.ROW_BYTES, sp["H"], sp["K"], sp["S"],
+                              dense=sp["dense"], extra_page=sp["E"]))
+        seq = []
+        for c in range(sp["n"]):
+            S = int(rng.integers(1, sp["S"] + 1))
+            topk = rng.integers(-2, sp["L"] + 2, size=(sp["B"], S, sp["K"])).astype(np.int32)
+            if seq:  # half of the first step repeats the previous call's last step
+                topk[:, 0, :sp["K"] // 2] = seq[-1][0][:, -1, :sp["K"] // 2]
+            rpi = rng.permutation(sp["R"])[:sp["B"]].astype(np.int32)
+            sl = rng.integers(sp["L"] // 2, sp["L"] + 1, size=sp["B"]).astype(np.int32)
+            seq.append((topk, rpi, sl))
+        calls.append(seq)
+        ins.append([(torch.from_numpy(r).cuda(), torch.from_numpy(s).cuda(),
+                     torch.from_numpy(t).cuda()) for t, r, s in seq])
+        outs.append([{"device_locs": torch.empty(t.shape, dtype=torch.int32, device="cuda"),
+                      "stats": torch.empty((t.shape[0], B.HS_NUM_STATS), dtype=torch.int32,
+                                           device="cuda")} for t, _, _ in seq])
+    torch.cuda.synchronize()
+    start = threading.Barrier(2)
+    errors = []
+
+    def drive(i):
+        try:
+            s = torch.cuda.Stream()
+            start.wait(timeout=60)
+            for (rpi, sl, topk), o in zip(ins[i], outs[i]):
+                runs[i].cache.swap_in(rpi, sl, topk, 0, out=o, stream=s)
+            s.synchronize()
+        except BaseException as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=drive, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not any(t.is_alive() for t in threads)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for i, run in enumerate(runs):
+        for c, ((topk, rpi, sl), o) in enumerate(zip(calls[i], outs[i])):
+            ref = run.oracle.swap_in(0, run.opools[0], run.mirror[0], rpi, sl, topk,
+                                     want_plan=False, num_threads=8)
+            assert (o["device_locs"].cpu().numpy() == ref["locs"]).all(), (i, c)
+            assert (o["stats"].cpu().numpy() == ref["stats"]).all(), (i, c)
+        got = run.cache.device_kv[0].cpu().numpy()
+        assert (got == run.mirror[0]).all(), i
+        for q in range(run.R):
+            gs, os_ = run.gpu_state(0, q), run.oracle.request_state(0, q)
+            for k in ("tok", "ep", "phys"):
+                assert (gs[k] == os_[k]).all(), (i, q, k)
+        assert run.cache.status()[1] == 0
