@@ -927,7 +927,7 @@ def main():
         "deferred_copy_pipeline": pipeline,
         "clocks": clk,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # the oracle baseline: N = 1 only
         line["cpu_baseline"] = cpu_baseline_oracle(w, calls, rpi_np, sl_np, args.cpu_seconds,
                                                    pool.numpy())
     if rank == 0:
