@@ -159,12 +159,48 @@ def _stream_ptr(stream) -> int:
     import torch
     if stream is None:
         stream = torch.cuda.current_stream()
+    want = getattr(_call_device, "index", None)
+    if want is not None and stream.device.index != want:
+        raise ValueError("the stream is on cuda:%d, the call runs on cuda:%d"
+                         % (stream.device.index, want))
     return int(stream.cuda_stream)
+
+
+_call_device = threading.local()  # device of the handle whose call is being marshalled
+
+
+class _on_device:
+    """Makes device `index` current for one library call (a handle's calls
+    must be made on its own device) and has _dptr and _stream_ptr reject
+    device tensors and streams of another device.  `index` None checks and
+    switches nothing."""
+
+    def __init__(self, index: Optional[int]):
+        self.index = index
+
+    def __enter__(self):
+        import torch
+        self.outer = getattr(_call_device, "index", None)
+        _call_device.index = self.index
+        self.prev = None
+        if self.index is not None and torch.cuda.is_available():
+            prev = torch.cuda.current_device()
+            if prev != self.index:
+                torch.cuda.set_device(self.index)
+                self.prev = prev
+        return self
+
+    def __exit__(self, *exc):
+        _call_device.index = self.outer
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _dptr(t, dtype=None, name="tensor") -> int:
     """Address of a tensor the kernels read or write: device memory, or pinned
-    (mapped) host memory, which the device addresses directly."""
+    (mapped) host memory, which the device addresses directly.  Inside
+    _on_device, a device tensor must be on that device."""
     if t is None:
         return 0
     if not t.is_contiguous():
@@ -173,6 +209,10 @@ def _dptr(t, dtype=None, name="tensor") -> int:
         raise ValueError("%s must have dtype %s" % (name, dtype))
     if not (t.is_cuda or t.is_pinned()):
         raise ValueError("%s must be in device memory or pinned host memory" % name)
+    want = getattr(_call_device, "index", None)
+    if t.is_cuda and want is not None and t.device.index != want:
+        raise ValueError("%s is on cuda:%d, the call runs on cuda:%d" % (name, t.device.index,
+                                                                        want))
     return int(t.data_ptr())
 
 
@@ -249,9 +289,10 @@ def hs_status_string(code: int) -> str:
 class StateHandle:
     """Owns the library's host handle; keeps the caller's tensors alive."""
 
-    def __init__(self, ptr: int, cfg: HsConfig, keep: Sequence):
+    def __init__(self, ptr: int, cfg: HsConfig, keep: Sequence, device: int):
         self.ptr = ctypes.c_void_p(ptr)
         self.cfg = cfg
+        self.device = device  # the CUDA device the handle and its buffers are on
         self._keep = list(keep)
 
     def close(self) -> None:
@@ -272,16 +313,22 @@ def hs_create_state(cfg: HsConfig, host_pools: Sequence, device_kvs: Sequence, s
     L = cfg.num_layers
     if len(host_pools) != L or len(device_kvs) != L:
         raise ValueError("need one host pool and one device KV buffer per layer")
-    hp = (ctypes.c_void_p * L)(*[_hptr(t, name="host pool") for t in host_pools])
-    dk = (ctypes.c_void_p * L)(*[_dptr(t, name="device kv") for t in device_kvs])
-    out = ctypes.c_void_p()
-    rc = lib.hs_create_state(ctypes.byref(cfg), ctypes.cast(hp, _vp), ctypes.cast(dk, _vp),
-                             _dptr(state, name="state"), state.numel() * state.element_size(),
-                             _dptr(workspace, name="workspace"),
-                             workspace.numel() * workspace.element_size(), _stream_ptr(stream),
-                             ctypes.byref(out))
+    # The handle belongs to the device that holds its device buffers.
+    if not state.is_cuda:
+        raise ValueError("state must be in device memory")
+    device = state.device.index
+    with _on_device(device):
+        hp = (ctypes.c_void_p * L)(*[_hptr(t, name="host pool") for t in host_pools])
+        dk = (ctypes.c_void_p * L)(*[_dptr(t, name="device kv") for t in device_kvs])
+        out = ctypes.c_void_p()
+        rc = lib.hs_create_state(ctypes.byref(cfg), ctypes.cast(hp, _vp), ctypes.cast(dk, _vp),
+                                 _dptr(state, name="state"), state.numel() * state.element_size(),
+                                 _dptr(workspace, name="workspace"),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream), ctypes.byref(out))
     _check(rc, "hs_create_state")
-    return StateHandle(out.value, cfg, list(host_pools) + list(device_kvs) + [state, workspace])
+    return StateHandle(out.value, cfg, list(host_pools) + list(device_kvs) + [state, workspace],
+                       device)
 
 
 def hs_destroy_state(handle: StateHandle) -> None:
@@ -294,14 +341,15 @@ def hs_swap_in(handle: StateHandle, req_pool_indices, seq_lens, topk, layer_id: 
     import torch
     B, S, K = _swap_in_shapes(handle, req_pool_indices, seq_lens, topk, device_locs, stats,
                               miss_src, miss_dst, miss_count)
-    rc = load_library().hs_swap_in(
-        handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
-        _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
-        layer_id, _dptr(device_locs, torch.int32, "device_locs"),
-        _dptr(stats, torch.int32, "stats"), _dptr(miss_src, torch.int64, "miss_src"),
-        _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
-        _stream_ptr(stream))
-    _check(rc, "hs_swap_in")
+    with _on_device(handle.device):
+        rc = load_library().hs_swap_in(
+            handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
+            _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
+            layer_id, _dptr(device_locs, torch.int32, "device_locs"),
+            _dptr(stats, torch.int32, "stats"), _dptr(miss_src, torch.int64, "miss_src"),
+            _dptr(miss_dst, torch.int64, "miss_dst"),
+            _dptr(miss_count, torch.int32, "miss_count"), _stream_ptr(stream))
+        _check(rc, "hs_swap_in")
 
 
 def hs_page_table(topk, seq_lens, max_seq_len: int, page_size: int, pages, num_pages,
@@ -314,30 +362,34 @@ def hs_page_table(topk, seq_lens, max_seq_len: int, page_size: int, pages, num_p
     _shape(pages, (B, S * K), "pages")
     _shape(num_pages, (B,), "num_pages")
     _shape(token_page, (B, S, K), "token_page")
-    rc = load_library().hs_page_table(
-        _dptr(topk, torch.int32, "topk"), _dptr(seq_lens, torch.int32, "seq_lens"), B, S, K,
-        max_seq_len, page_size, _dptr(pages, torch.int32, "pages"),
-        _dptr(num_pages, torch.int32, "num_pages"), _dptr(token_page, torch.int32, "token_page"),
-        _stream_ptr(stream))
-    _check(rc, "hs_page_table")
+    # runs on the device of its inputs (the current device for pinned host inputs)
+    with _on_device(topk.device.index if topk.is_cuda else None):
+        rc = load_library().hs_page_table(
+            _dptr(topk, torch.int32, "topk"), _dptr(seq_lens, torch.int32, "seq_lens"), B, S, K,
+            max_seq_len, page_size, _dptr(pages, torch.int32, "pages"),
+            _dptr(num_pages, torch.int32, "num_pages"), _dptr(token_page, torch.int32, "token_page"),
+            _stream_ptr(stream))
+        _check(rc, "hs_page_table")
 
 
 def hs_reset_requests(handle: StateHandle, req_pool_indices, stream=None) -> None:
     import torch
     if req_pool_indices.dim() != 1:
         raise ValueError("req_pool_indices must be 1-D")
-    rc = load_library().hs_reset_requests(
-        handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
-        req_pool_indices.numel(), _stream_ptr(stream))
-    _check(rc, "hs_reset_requests")
+    with _on_device(handle.device):
+        rc = load_library().hs_reset_requests(
+            handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
+            req_pool_indices.numel(), _stream_ptr(stream))
+        _check(rc, "hs_reset_requests")
 
 
 def hs_get_status(handle: StateHandle, stream=None):
     """Returns (code, flags); synchronises the stream and clears the flags."""
     flags = ctypes.c_uint32(0)
-    rc = load_library().hs_get_status(handle.ptr, ctypes.byref(flags), _stream_ptr(stream))
-    if rc not in (HS_OK, HS_ERR_DEVICE_STATUS):
-        _check(rc, "hs_get_status")
+    with _on_device(handle.device):
+        rc = load_library().hs_get_status(handle.ptr, ctypes.byref(flags), _stream_ptr(stream))
+        if rc not in (HS_OK, HS_ERR_DEVICE_STATUS):
+            _check(rc, "hs_get_status")
     return rc, flags.value
 
 
@@ -353,10 +405,11 @@ def hs_export_request_state(handle: StateHandle, layer_id: int, request: int, st
     # hash entries, or the dense map widened to int64 [max_seq_len]
     bank = np.empty(cfg.max_seq_len if cfg.index_kind == HS_INDEX_DENSE else hs_hash_size(cfg),
                     np.int64)
-    rc = load_library().hs_export_request_state(
-        handle.ptr, layer_id, request, tok.ctypes.data, ep.ctypes.data, phys.ctypes.data,
-        ctrl.ctypes.data, bank.ctypes.data, _stream_ptr(stream))
-    _check(rc, "hs_export_request_state")
+    with _on_device(handle.device):
+        rc = load_library().hs_export_request_state(
+            handle.ptr, layer_id, request, tok.ctypes.data, ep.ctypes.data, phys.ctypes.data,
+            ctrl.ctypes.data, bank.ctypes.data, _stream_ptr(stream))
+        _check(rc, "hs_export_request_state")
     return {"tok": tok, "ep": ep, "phys": phys, "ctrl": ctrl, "bank": bank,
             "epoch": int(ctrl[0])}
 
@@ -371,20 +424,22 @@ def hs_append_rows(handle: StateHandle, layer_id: int, req, tok, seq_lens, rows,
     _shape(tok, (n,), "tok")
     _shape(seq_lens, (n,), "seq_lens")
     _shape(rows, (n, handle.cfg.item_size_bytes), "rows")
-    rc = load_library().hs_append_rows(
-        handle.ptr, layer_id, _dptr(req, torch.int32, "req"), _dptr(tok, torch.int32, "tok"),
-        _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(rows, torch.uint8, "rows"), n,
-        _stream_ptr(stream))
-    _check(rc, "hs_append_rows")
+    with _on_device(handle.device):
+        rc = load_library().hs_append_rows(
+            handle.ptr, layer_id, _dptr(req, torch.int32, "req"), _dptr(tok, torch.int32, "tok"),
+            _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(rows, torch.uint8, "rows"), n,
+            _stream_ptr(stream))
+        _check(rc, "hs_append_rows")
 
 
 def hs_get_stats(handle: StateHandle, layer_id: int, reset: bool = False, stream=None):
     """Running sums of the HS_STAT_* counters of one layer: int64 [HS_NUM_STATS]."""
     import numpy as np
     out = np.zeros(HS_NUM_STATS, dtype=np.int64)
-    rc = load_library().hs_get_stats(handle.ptr, layer_id, out.ctypes.data, 1 if reset else 0,
-                                     _stream_ptr(stream))
-    _check(rc, "hs_get_stats")
+    with _on_device(handle.device):
+        rc = load_library().hs_get_stats(handle.ptr, layer_id, out.ctypes.data, 1 if reset else 0,
+                                         _stream_ptr(stream))
+        _check(rc, "hs_get_stats")
     return out
 
 
@@ -410,11 +465,12 @@ def hs_copy_planned(handle: StateHandle, layer_id: int, miss_src, miss_dst, miss
     _shape(miss_count, (B,), "miss_count")
     _shape(miss_src, (B, C), "miss_src")
     _shape(miss_dst, (B, C), "miss_dst")
-    rc = load_library().hs_copy_planned(
-        handle.ptr, layer_id, _dptr(miss_src, torch.int64, "miss_src"),
-        _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
-        miss_count.numel(), _stream_ptr(stream))
-    _check(rc, "hs_copy_planned")
+    with _on_device(handle.device):
+        rc = load_library().hs_copy_planned(
+            handle.ptr, layer_id, _dptr(miss_src, torch.int64, "miss_src"),
+            _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
+            miss_count.numel(), _stream_ptr(stream))
+        _check(rc, "hs_copy_planned")
 
 
 def hs_swap_in_noalloc(handle: StateHandle, req_pool_indices, seq_lens, topk, layer_id: int,
@@ -425,11 +481,12 @@ def hs_swap_in_noalloc(handle: StateHandle, req_pool_indices, seq_lens, topk, la
     import torch
     B, S, K = _swap_in_shapes(handle, req_pool_indices, seq_lens, topk, device_locs, stats,
                               miss_src, miss_dst, miss_count)
-    rc = load_library().hs_swap_in_noalloc(
-        handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
-        _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
-        layer_id, _dptr(device_locs, torch.int32, "device_locs"),
-        _dptr(stats, torch.int32, "stats"), _dptr(miss_src, torch.int64, "miss_src"),
-        _dptr(miss_dst, torch.int64, "miss_dst"), _dptr(miss_count, torch.int32, "miss_count"),
-        _stream_ptr(stream))
-    _check(rc, "hs_swap_in_noalloc")
+    with _on_device(handle.device):
+        rc = load_library().hs_swap_in_noalloc(
+            handle.ptr, _dptr(req_pool_indices, torch.int32, "req_pool_indices"),
+            _dptr(seq_lens, torch.int32, "seq_lens"), _dptr(topk, torch.int32, "topk"), B, S,
+            layer_id, _dptr(device_locs, torch.int32, "device_locs"),
+            _dptr(stats, torch.int32, "stats"), _dptr(miss_src, torch.int64, "miss_src"),
+            _dptr(miss_dst, torch.int64, "miss_dst"),
+            _dptr(miss_count, torch.int32, "miss_count"), _stream_ptr(stream))
+        _check(rc, "hs_swap_in_noalloc")

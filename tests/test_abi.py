@@ -176,6 +176,7 @@ def test_binding_checks_shapes_and_memory_before_any_launch():
 
     class Handle:  # never reaches the library: every call below fails first
         ptr = None
+        device = 0
         cfg = _cfg(num_requests=8, max_seq_len=100, hot_buffer_size=16, top_k=4, max_steps=2,
                    max_batch=8)
 
@@ -204,3 +205,38 @@ def test_binding_checks_shapes_and_memory_before_any_launch():
     with pytest.raises(ValueError, match="token_page"):
         B.hs_page_table(topk, rpi, 100, 16, torch.zeros((2, 4), **i32), rpi,
                         torch.zeros((2, 4), **i32))
+
+
+def test_binding_rejects_tensors_and_streams_of_another_device():
+    """A handle's calls run on its own device: inside a call for cuda:0 the
+    binding refuses a device tensor or a stream that lives on cuda:1 (checked
+    with stand-in objects, so no GPU is needed)."""
+    import torch
+
+    class OnCuda1:
+        is_cuda = True
+        dtype = torch.int32
+        device = torch.device("cuda", 1)
+
+        def is_contiguous(self):
+            return True
+
+        def is_pinned(self):
+            return False
+
+        def data_ptr(self):
+            return 0x10000
+
+    class Stream1:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    with B._on_device(1):  # no switch without a GPU; checks only
+        assert B._dptr(OnCuda1(), torch.int32, "x") == 0x10000
+        assert B._stream_ptr(Stream1()) == 0
+    with B._on_device(0):
+        with pytest.raises(ValueError, match="cuda:1"):
+            B._dptr(OnCuda1(), torch.int32, "topk")
+        with pytest.raises(ValueError, match="stream"):
+            B._stream_ptr(Stream1())
+    assert B._dptr(OnCuda1(), torch.int32, "x") == 0x10000  # outside a call: no device rule

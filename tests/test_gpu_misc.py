@@ -295,3 +295,19 @@ def test_two_handles_concurrent_threads_and_streams():
             for k in ("tok", "ep", "phys"):
                 assert (gs[k] == os_[k]).all(), (i, q, k)
         assert run.cache.status()[1] == 0
+
+
+def test_handle_is_bound_to_its_buffers_device():
+    """The binding binds a handle to the device of its device buffers and runs
+    each call with that device current."""
+    cfg = pkg.make_config(2, 300, W.ROW_BYTES, 16, 8, 1, 1)
+    from sparse_attention_kv_swap_gb300.cache import SwapInCache
+    cache = SwapInCache(cfg, device=torch.device("cuda", 0))
+    assert cache.handle.device == 0
+    i32 = dict(dtype=torch.int32, device="cuda:0")
+    out = cache.swap_in(torch.tensor([0, 1], **i32), torch.tensor([300, 300], **i32),
+                        torch.arange(16, **i32).view(2, 1, 8), 0, stats=True)
+    torch.cuda.synchronize()
+    assert (out["device_locs"].cpu().numpy() >= 0).all()
+    assert cache.status()[1] == 0
+    cache.close()
