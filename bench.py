@@ -104,14 +104,25 @@ class ClockSampler:
     def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.samples = []
         self.proc = None
-        self.gpu = gpu_index
+        self.gpu = self.smi_id(gpu_index)
         self.interval = interval_ms
         self.thread = None
+
+    @staticmethod
+    def smi_id(gpu_index: int) -> str:
+        """nvidia-smi's name for torch device `gpu_index`: its UUID, which stays
+        right when CUDA_VISIBLE_DEVICES renumbers the devices (else the index)."""
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(gpu_index)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                ["nvidia-smi", "-i", self.gpu, "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
