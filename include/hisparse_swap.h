@@ -26,6 +26,9 @@
  *    A device pointer may also address mapped pinned host memory (with
  *    unified addressing, the pinned buffer's own address): the kernels then
  *    read or write it across the host link, e.g. NVLink-C2C on Grace.
+ *    Arrays must be aligned to their element type (4 bytes for int32_t, 8
+ *    for int64_t); a misaligned one returns HS_ERR_INVALID_ARG before any
+ *    launch.
  *    The caller owns every buffer (pinned host pool, device KV buffers,
  *    state, workspace, inputs, outputs).  The library owns only the small
  *    host handle `hs_state`.  Buffer sizes follow from the config and the

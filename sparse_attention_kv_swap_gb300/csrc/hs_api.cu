@@ -263,6 +263,11 @@ int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t*
     if (batch == 0) return HS_OK;
     if (!req_pool_indices_dev || !seq_lens_dev || !topk_dev || !device_locs_dev)
         return HS_ERR_INVALID_ARG;
+    if (!null_or_aligned(req_pool_indices_dev, 4) || !null_or_aligned(seq_lens_dev, 4) ||
+        !null_or_aligned(topk_dev, 4) || !null_or_aligned(device_locs_dev, 4) ||
+        !null_or_aligned(stats_dev, 4) || !null_or_aligned(miss_count_dev, 4) ||
+        !null_or_aligned(miss_src_dev, 8) || !null_or_aligned(miss_dst_dev, 8))
+        return HS_ERR_INVALID_ARG;
 
     SwapArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -297,7 +302,9 @@ int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
     const Dims& d = st->d;
     if (layer_id < 0 || layer_id >= d.layers || n < 0) return HS_ERR_INVALID_ARG;
     if (n == 0) return HS_OK;
-    if (!req_dev || !tok_dev || !seq_lens_dev || !rows_dev || !aligned(rows_dev, 16))
+    if (!req_dev || !tok_dev || !seq_lens_dev || !rows_dev || !aligned(rows_dev, 16) ||
+        !null_or_aligned(req_dev, 4) || !null_or_aligned(tok_dev, 4) ||
+        !null_or_aligned(seq_lens_dev, 4))
         return HS_ERR_INVALID_ARG;
     const LayerView lv = layer_view(d, st->state, layer_id, st->host_pool_dev[layer_id],
                                     st->device_kv[layer_id]);
@@ -328,6 +335,9 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
         return HS_ERR_INVALID_ARG;
     if (batch == 0) return HS_OK;
     if (!miss_src_dev || !miss_dst_dev || !miss_count_dev) return HS_ERR_INVALID_ARG;
+    if (!null_or_aligned(miss_src_dev, 8) || !null_or_aligned(miss_dst_dev, 8) ||
+        !null_or_aligned(miss_count_dev, 4))
+        return HS_ERR_INVALID_ARG;
     return launch_planned_copy(reinterpret_cast<const long long*>(miss_src_dev),
                                reinterpret_cast<const long long*>(miss_dst_dev), miss_count_dev,
                                batch, d.C, d.W, st->host_pool_dev[layer_id],
@@ -364,6 +374,10 @@ int hs_page_table(const int32_t* topk_dev, const int32_t* seq_lens_dev, int32_t 
     if (batch == 0) return HS_OK;
     if (!topk_dev || !seq_lens_dev || !pages_dev || !num_pages_dev || !token_page_dev)
         return HS_ERR_INVALID_ARG;
+    if (!null_or_aligned(topk_dev, 4) || !null_or_aligned(seq_lens_dev, 4) ||
+        !null_or_aligned(pages_dev, 4) || !null_or_aligned(num_pages_dev, 4) ||
+        !null_or_aligned(token_page_dev, 4))
+        return HS_ERR_INVALID_ARG;
     return launch_page_table(topk_dev, seq_lens_dev, batch, num_steps, top_k, max_seq_len,
                              page_size, pages_dev, num_pages_dev, token_page_dev,
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -376,7 +390,8 @@ int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t
     if (!st || n < 0) return HS_ERR_INVALID_ARG;
     if (!on_handle_device(st)) return HS_ERR_INVALID_ARG;
     if (n == 0) return HS_OK;
-    if (!req_pool_indices_dev || n > st->d.R) return HS_ERR_INVALID_ARG;
+    if (!req_pool_indices_dev || n > st->d.R || !null_or_aligned(req_pool_indices_dev, 4))
+        return HS_ERR_INVALID_ARG;
     return launch_reset(st->d, st->state, req_pool_indices_dev, n,
                         static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HS_OK

@@ -249,6 +249,12 @@ struct hs_state {
     int defer_copy;           // 1: hs_swap_in records the miss plan but copies nothing
 };
 
+// True for a null pointer or one aligned to `bytes` (the element size of an
+// int32 or int64 argument; the kernels load these arrays element by element).
+inline bool null_or_aligned(const void* p, size_t bytes) {
+    return ((uintptr_t)p % bytes) == 0;
+}
+
 // True when the calling thread's current device is the one the handle was
 // created on.  Every entry point that launches or copies checks it, so that a
 // call made while another device is current fails instead of running there.

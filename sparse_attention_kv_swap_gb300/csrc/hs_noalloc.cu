@@ -73,6 +73,11 @@ extern "C" int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_
     if (batch == 0) return HS_OK;
     if (!req_pool_indices_dev || !seq_lens_dev || !topk_dev || !device_locs_dev)
         return HS_ERR_INVALID_ARG;
+    if (!null_or_aligned(req_pool_indices_dev, 4) || !null_or_aligned(seq_lens_dev, 4) ||
+        !null_or_aligned(topk_dev, 4) || !null_or_aligned(device_locs_dev, 4) ||
+        !null_or_aligned(stats_dev, 4) || !null_or_aligned(miss_count_dev, 4) ||
+        !null_or_aligned(miss_src_dev, 8) || !null_or_aligned(miss_dst_dev, 8))
+        return HS_ERR_INVALID_ARG;
 
     int device = -1;
     if (cudaGetDevice(&device) != cudaSuccess) return HS_ERR_CUDA;

@@ -120,6 +120,13 @@ def test_page_table_rejects_bad_arguments(lib):
     assert lib.hs_page_table(None, None, 0, 1, 4, 100, 16, None, None, None, None) == B.HS_OK
     assert lib.hs_page_table(None, None, 2, 1, 4, 100, 16, None, None, None, None) == \
         B.HS_ERR_INVALID_ARG
+    # int32 arrays must be 4-byte aligned: a misaligned address is refused on the
+    # host (the addresses below are never dereferenced)
+    ok, odd = 0x20000, 0x20002
+    for bad in range(5):
+        ptrs = [odd if i == bad else ok + 0x1000 * i for i in range(5)]
+        assert lib.hs_page_table(ptrs[0], ptrs[1], 2, 1, 4, 100, 16, ptrs[2], ptrs[3],
+                                 ptrs[4], None) == B.HS_ERR_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(tmp_path):
