@@ -51,6 +51,14 @@ MUTANTS = {
                             "if (o->E > 0)"),
     "append_skips_host": ("std::memcpy(host_pool + ((int64_t)q * o->L + t) * W, row, (size_t)W);",
                           ";"),
+    "hit_location_ignores_rotation": ("locs_b[i] = (int32_t)(base + rc.phys[v]);",
+                                      "locs_b[i] = (int32_t)(base + v);"),
+    "page_offset_dropped": ("? index[t / page_size] * page_size + t % page_size",
+                            "? index[t / page_size] * page_size"),
+    "invalid_not_counted": ("stat[HSO_STAT_INVALID]++;", ""),
+    "overflow_tie_prefers_later_miss": ("return last_step[a] > last_step[b];\n            return a < b;",
+                                        "return last_step[a] > last_step[b];\n            return a > b;"),
+    "duplicate_misses_not_merged": ("auto f = first.find(t);", "auto f = first.end();"),
 }
 
 
