@@ -235,3 +235,47 @@ def test_batches_wider_than_the_gpu(B, S, K):
     run = ParityRun(R, L, W.ROW_BYTES, H, K, S, max_batch=B)
     for topk, rpi, sl in _rand_calls(rng, R, L, K, S, B, 4):
         run.call(topk, rpi, sl, properties=False)
+
+
+def test_long_run_epochs_beyond_sixteen_bits():
+    """65,600 calls on a 4-slot cache, both requests in every call: the epoch
+    passes 2^8 and 2^16, so the commit's victim selection runs its radix
+    select with two and then three digit passes.  Every call's locations and
+    counters, and the final policy state and rows, equal the oracle's."""
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    R, L, Wd, H, K, N = 2, 64, 16, 4, 3, 65600
+    run = ParityRun(R, L, Wd, H, K, 1)
+    rng = np.random.default_rng(77)
+    topk = rng.integers(0, 16, size=(N, R, 1, K)).astype(np.int32)
+    topk[rng.random(topk.shape) < 0.02] = -1
+    rpi = np.arange(R, dtype=np.int32)
+    sl = np.full(R, L, dtype=np.int32)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    topk_d = torch.from_numpy(topk).cuda()
+    rpi_d, sl_d = torch.from_numpy(rpi).cuda(), torch.from_numpy(sl).cuda()
+    locs_d = torch.empty((N, R, 1, K), **i32)
+    stats_d = torch.empty((N, R, pkg.binding.HS_NUM_STATS), **i32)
+    for i in range(N):
+        run.cache.swap_in(rpi_d, sl_d, topk_d[i], 0,
+                          out={"device_locs": locs_d[i], "stats": stats_d[i]})
+    want_locs = np.empty((N, R, 1, K), dtype=np.int32)
+    want_stats = np.empty((N, R, pkg.binding.HS_NUM_STATS), dtype=np.int32)
+    for i in range(N):
+        ref = run.oracle.swap_in(0, run.opools[0], run.mirror[0], rpi, sl, topk[i])
+        want_locs[i], want_stats[i] = ref["locs"], ref["stats"]
+    torch.cuda.synchronize()
+    assert run.cache.status()[1] == 0
+    got_locs, got_stats = locs_d.cpu().numpy(), stats_d.cpu().numpy()
+    bad = np.argwhere((got_locs != want_locs).reshape(N, -1).any(axis=1))
+    assert bad.size == 0, "locations differ from call %d on" % bad[0][0]
+    bad = np.argwhere((got_stats != want_stats).reshape(N, -1).any(axis=1))
+    assert bad.size == 0, "counters differ from call %d on" % bad[0][0]
+    evicted = 5  # HS_STAT_EVICTED
+    assert want_stats[:, :, evicted].sum() > N  # the cache kept evicting throughout
+    for q in range(R):
+        gs, os_ = run.gpu_state(0, q), run.oracle.request_state(0, q)
+        assert gs["epoch"] == os_["epoch"] == N
+        for k in ("tok", "ep", "phys"):
+            assert (gs[k] == os_[k]).all(), (q, k)
+    assert (run.cache.device_kv[0].cpu().numpy() == run.mirror[0]).all()
