@@ -20,6 +20,10 @@ AssertionError on a mismatch.
   pin_extra_reduction: an extra-page cache behaves exactly like a cache
                       without one that is shown the same calls with the
                       extra-page entries blanked out;
+  pin_reset:          random calls over two layers with requests reset in
+                      between equal the brute-force list model, in which a
+                      reset request simply starts a new empty cache in every
+                      layer (other requests untouched);
   pin_append_decode:  a decode loop that appends every new token's row and
                       rewrites some older ones: every returned row and
                       every resident row equals the latest row written for
@@ -160,6 +164,42 @@ def pin_simulator(lib, trials: int = 25, calls: int = 8) -> None:
                 assert st["ep"].tolist() == sims[q].ep
                 assert st["phys"].tolist() == sims[q].phys
                 assert st["epoch"] == sims[q].epoch
+
+
+def pin_reset(lib, trials: int = 12, calls: int = 10) -> None:
+    rng = np.random.default_rng(29)
+    for trial in range(trials):
+        H = int(rng.integers(1, 7))
+        K = int(rng.integers(1, 7))
+        S_max = int(rng.integers(1, 4))
+        R = int(rng.integers(2, 5))
+        L = 16
+        h = OracleHarness(R, L, WIDTH, H, K, S_max, layers=2, lib=lib)
+        sims = {(l, q): ListCache(H, S_max * K) for l in range(2) for q in range(R)}
+        for c in range(calls):
+            if c and rng.random() < 0.4:
+                gone = rng.permutation(R)[:int(rng.integers(1, R))].astype(np.int32)
+                h.o.reset_requests(gone)
+                for q in gone.tolist():
+                    for l in range(2):
+                        sims[(l, q)] = ListCache(H, S_max * K)
+            B = int(rng.integers(1, R + 1))
+            S = int(rng.integers(1, S_max + 1))
+            layer = int(rng.integers(0, 2))
+            topk, rpi, sl = _random_call(rng, B, R, S, K, L)
+            out = h.call(topk, rpi, sl, layer=layer, check=False)
+            for b in range(B):
+                q = int(rpi[b])
+                locs, stats = sims[(layer, q)].call(q, topk[b].tolist(), min(int(sl[b]), L))
+                assert out["locs"][b].tolist() == locs, "locations differ after a reset"
+                assert out["stats"][b].tolist() == stats, "counters differ after a reset"
+            for l in range(2):
+                for q in range(R):
+                    st = h.o.request_state(l, q)
+                    assert st["tok"].tolist() == sims[(l, q)].tok
+                    assert st["ep"].tolist() == sims[(l, q)].ep
+                    assert st["phys"].tolist() == sims[(l, q)].phys
+                    assert st["epoch"] == sims[(l, q)].epoch
 
 
 def pin_overflow(lib) -> None:
@@ -331,4 +371,4 @@ def pin_append_decode(lib, trials: int = 6, steps: int = 24) -> None:
 
 ALL_PINS = (pin_lru, pin_first_call, pin_repeat_call, pin_invariants, pin_simulator,
             pin_overflow, pin_782, pin_page_table, pin_extra_simulator, pin_extra_reduction,
-            pin_append_decode)
+            pin_append_decode, pin_reset)

@@ -59,6 +59,12 @@ MUTANTS = {
     "overflow_tie_prefers_later_miss": ("return last_step[a] > last_step[b];\n            return a < b;",
                                         "return last_step[a] > last_step[b];\n            return a > b;"),
     "duplicate_misses_not_merged": ("auto f = first.find(t);", "auto f = first.end();"),
+    "reset_first_layer_only": (
+        "for (int32_t l = 0; l < o->layers; ++l) make_empty(*o, o->at(l, req_pool_indices[i]));",
+        "make_empty(*o, o->at(0, req_pool_indices[i]));"),
+    "reset_skips_first_request": (
+        "    for (int32_t i = 0; i < n; ++i)\n        for (int32_t l = 0; l < o->layers; ++l)",
+        "    for (int32_t i = 1; i < n; ++i)\n        for (int32_t l = 0; l < o->layers; ++l)"),
 }
 
 
