@@ -6,7 +6,8 @@ AssertionError on a mismatch.
 
   pin_lru:            with one token per call, epoch-CLOCK with a lowest-slot
                       tie-break must equal textbook LRU (an OrderedDict);
-  pin_first_call:     closed forms of the first call on an empty cache;
+  pin_first_call:     closed forms of the first call on an empty cache,
+                      including its miss plan;
   pin_repeat_call:    repeating a call that fits is all hits, same locations;
   pin_invariants:     random tiny sweeps checked with the property checker;
   pin_simulator:      random tiny sweeps equal the brute-force list model;
@@ -76,13 +77,18 @@ def pin_first_call(lib) -> None:
         topk = rng.integers(-3, L + 3, size=(2, S, K)).astype(np.int32)
         rpi = np.array([2, 0], np.int32)
         sl = np.array([L, 30], np.int32)
-        out = h.call(topk, rpi, sl)
+        out = h.call(topk, rpi, sl, want_plan=True)
         for b in range(2):
             q = int(rpi[b])
             flat = topk[b].reshape(-1)
             valid = [t for t in flat.tolist() if 0 <= t < sl[b]]
             distinct = list(dict.fromkeys(valid))
             assert out["stats"][b][3] == len(distinct)
+            # the miss plan: host row (q, t_j) -> scratch row j, one per unique miss
+            U = len(distinct)
+            assert out["miss_count"][b] == U
+            assert out["miss_src"][b][:U].tolist() == [q * L + t for t in distinct]
+            assert out["miss_dst"][b][:U].tolist() == [q * (H + C) + H + j for j in range(U)]
             first = {t: j for j, t in enumerate(distinct)}
             for i, t in enumerate(flat.tolist()):
                 want = q * (H + C) + H + first[t] if t in first else -1

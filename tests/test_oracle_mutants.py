@@ -59,6 +59,9 @@ MUTANTS = {
     "overflow_tie_prefers_later_miss": ("return last_step[a] > last_step[b];\n            return a < b;",
                                         "return last_step[a] > last_step[b];\n            return a > b;"),
     "duplicate_misses_not_merged": ("auto f = first.find(t);", "auto f = first.end();"),
+    "plan_source_is_destination": ("if (src_b) src_b[j] = src_row;", "if (src_b) src_b[j] = dst_row;"),
+    "plan_count_off_by_one": ("if (count_b) *count_b = (int32_t)U.size();",
+                              "if (count_b) *count_b = (int32_t)U.size() - 1;"),
     "reset_first_layer_only": (
         "for (int32_t l = 0; l < o->layers; ++l) make_empty(*o, o->at(l, req_pool_indices[i]));",
         "make_empty(*o, o->at(0, req_pool_indices[i]));"),
