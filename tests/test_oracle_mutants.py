@@ -62,6 +62,8 @@ MUTANTS = {
     "plan_source_is_destination": ("if (src_b) src_b[j] = src_row;", "if (src_b) src_b[j] = dst_row;"),
     "plan_count_off_by_one": ("if (count_b) *count_b = (int32_t)U.size();",
                               "if (count_b) *count_b = (int32_t)U.size() - 1;"),
+    "layers_share_one_cache": ("swap_in_request(*o, o->at(layer, q), q,",
+                               "swap_in_request(*o, o->at(0, q), q,"),
     "reset_first_layer_only": (
         "for (int32_t l = 0; l < o->layers; ++l) make_empty(*o, o->at(l, req_pool_indices[i]));",
         "make_empty(*o, o->at(0, req_pool_indices[i]));"),
