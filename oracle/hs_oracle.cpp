@@ -57,6 +57,16 @@
 //     request of length n writes host row (q, t); the extra-page row of t
 //     if t lies in the extra page of length n; and the hot row of t if t is
 //     resident, so that every copy of (q, t) stays equal.
+//
+// Pins (tests/pins.py, run by the CPU test-suite against this library and
+// against planted mistakes in copies of this file): textbook LRU at one
+// token per call; closed forms of a first call, its miss plan included; a
+// brute-force list model of readings 1-7 over random tiny calls, with
+// request resets and with the extra page; the page table against a plain
+// sorted unique of pages; and a plain dict of the latest row per (q, t)
+// through a decode loop with write-back.  The pages print no worked example,
+// so the exact slot numbering rests on readings 3-5, which the list model
+// restates independently.
 #include "hs_oracle.h"
 
 #include <algorithm>
