@@ -247,3 +247,23 @@ def test_binding_rejects_tensors_and_streams_of_another_device():
         with pytest.raises(ValueError, match="stream"):
             B._stream_ptr(Stream1())
     assert B._dptr(OnCuda1(), torch.int32, "x") == 0x10000  # outside a call: no device rule
+
+
+def test_product_path_never_reaches_the_oracle(lib):
+    """The package (Python and CUDA sources) neither imports, links, loads nor
+    names the CPU oracle, and the CUDA library exports none of its symbols:
+    every step of a swap-in runs in the library's kernels."""
+    import glob
+    import os
+    import re
+    pkg_dir = os.path.dirname(B.__file__)
+    files = (glob.glob(os.path.join(pkg_dir, "*.py"))
+             + glob.glob(os.path.join(pkg_dir, "csrc", "*.cu"))
+             + glob.glob(os.path.join(pkg_dir, "csrc", "*.cuh"))
+             + glob.glob(os.path.join(os.path.dirname(B.HEADER), "*.h")))
+    assert files
+    for path in files:
+        text = open(path).read()
+        assert not re.search(r"\boracle\b|hso_|hs_oracle", text, re.IGNORECASE), path
+    for sym in ("hso_create", "hso_swap_in", "hso_reset_requests"):
+        assert not hasattr(lib, sym), sym
