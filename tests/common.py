@@ -1,7 +1,7 @@
 """Shared helpers for the tests: host pools and oracle runs with checks."""
 from __future__ import annotations
 
-from typing import Dict, List, Optional
+from typing import Dict
 
 import numpy as np
 
