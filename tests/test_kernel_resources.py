@@ -3,7 +3,8 @@ needed).  No kernel may spill registers or keep a stack frame, and the
 kernels whose launch bounds promise full occupancy (the gather at 1024
 threads per SM, the commit + copy and planned-copy kernels at 2 x 512) must
 fit 64 registers a thread, so that the bounds hold without spilling.  A change
-that breaks either shows up here before it costs time on the GPU."""
+that breaks either shows up here before it costs time on the GPU.  The same
+sources, and the CPU oracle, also compile with warnings as errors."""
 import concurrent.futures as cf
 import os
 import re
@@ -80,3 +81,33 @@ def test_report_parser_reads_spills_and_registers():
         "ptxas info    : Used 12 registers, used 0 barriers",
     ])
     assert _parse(report) == {"_Z3fooPi": (16, 8, 4, 72), "_Z3barv": (0, 0, 0, 12)}
+
+
+def test_sources_compile_without_warnings(tmp_path):
+    """The CUDA sources (device and host code) and the CPU oracle compile with
+    every common warning turned into an error."""
+    import shutil
+    try:
+        nvcc = build._nvcc()
+    except Exception:
+        pytest.skip("no nvcc")
+    srcs = build._sources()
+
+    def one(src):
+        cmd = ([nvcc] + build.ARCH_FLAGS + build.NVCC_FLAGS
+               + ["-Werror", "all-warnings", "-Xcompiler", "-Wall,-Wextra,-Werror",
+                  "-I", build.INCLUDE, "-I", build.CSRC, "-c", src,
+                  "-o", str(tmp_path / (os.path.basename(src) + ".o"))])
+        return src, subprocess.run(cmd, capture_output=True, text=True)
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+        for src, res in ex.map(one, srcs):
+            assert res.returncode == 0, "%s:\n%s" % (src, res.stderr)
+    gxx = shutil.which("g++")
+    if gxx:
+        oracle_src = os.path.join(os.path.dirname(build.CSRC), "..", "oracle", "hs_oracle.cpp")
+        res = subprocess.run([gxx, "-std=c++17", "-O2", "-Wall", "-Wextra", "-Wpedantic",
+                              "-Werror", "-fPIC", "-shared", "-pthread",
+                              os.path.normpath(oracle_src), "-o", str(tmp_path / "o.so")],
+                             capture_output=True, text=True)
+        assert res.returncode == 0, res.stderr
