@@ -68,3 +68,16 @@ def test_config_names_the_workload_and_the_flush():
     assert "flushed" in c["l2"] and c["parallelism"] == "single GPU"
     assert bench.config_dict(w, 8)["parallelism"] == "replicas x8"
     assert not any(k in c for k in ("model", "global_batch"))  # a workload, not a model
+
+
+def test_cpu_baseline_times_the_oracle_on_a_bounded_sample():
+    import numpy as np
+    w = W.scaled(W.WORKLOADS["C2"], batch=2, seq_len=4096, top_k=256, hot_buffer=512)
+    calls = W.TopkStream(w).calls(bench.PREROLL_CALLS + 4)
+    pool = np.empty((w.batch, w.seq_len, w.row_bytes), dtype=np.uint8)
+    W.fill_host_pool(pool, 0)
+    out = bench.cpu_baseline_oracle(w, calls, W.req_pool_indices(w), W.seq_lens(w), 0.0, pool)
+    assert out["kind"] == "oracle" and out["unit"] == bench.UNIT
+    assert out["cores"] == min(w.batch, os.cpu_count() or 1)
+    assert out["value"] > 0 and "steady-state calls" in out["sample"]
+    assert out["sample"].startswith("2 ")  # at least two timed calls, even with no time budget
