@@ -107,11 +107,13 @@ extern "C" {
 #define HS_MAX_ENTRIES 8192      /* max_steps * top_k per request per call */
 #define HS_MAX_PAGES 262144      /* ceil(max_seq_len / page_size) for hs_page_table */
 #define HS_MAX_EXTRA_PAGE 65536  /* extra_page_size upper bound */
+#define HS_MAX_ITEM_BYTES 65536  /* item_size_bytes upper bound (MLA rows are 656) */
 
 typedef struct hs_config {
     int32_t num_requests;    /* R: request-pool slots (req_pool_indices range)    */
     int32_t max_seq_len;     /* L_max: host rows per request and layer            */
-    int32_t item_size_bytes; /* W: bytes per KV row; a multiple of 16 (656 = MLA) */
+    int32_t item_size_bytes; /* W: bytes per KV row; a multiple of 16, at most
+                                HS_MAX_ITEM_BYTES (656 = MLA)                     */
     int32_t hot_buffer_size; /* H: hot slots per request and layer, 1..32768      */
     int32_t top_k;           /* K: indices per request and step                   */
     int32_t max_steps;       /* S_max: 1..4 speculative steps                     */
@@ -209,8 +211,10 @@ void hs_destroy_state(hs_state* st);
  *   (the three miss-plan pointers are all NULL or all non-NULL; entries
  *    j >= U are left untouched)
  * Locations stay valid until the next call on the same layer (extra-page
- * locations: until hs_append_rows rewrites that row).  Launches two
- * kernels on `stream`; the second uses programmatic dependent launch. */
+ * locations: until hs_append_rows rewrites that row).  Launches one kernel
+ * on `stream`: each batch row's thread-block cluster looks up, de-duplicates
+ * and locates its entries, then commits the request's policy state while
+ * its other warps copy the request's miss rows. */
 int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t* seq_lens_dev,
                const int32_t* topk_dev, int32_t batch, int32_t num_steps, int32_t layer_id,
                int32_t* device_locs_dev, int32_t* stats_dev, int64_t* miss_src_dev,
@@ -315,15 +319,19 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
                     const int64_t* miss_dst_dev, const int32_t* miss_count_dev, int32_t batch,
                     void* stream);
 
-/* Profiling: when `event_host` (a cudaEvent_t) is non-NULL, every later
- * hs_swap_in on this handle records it on its stream between the gather
- * kernel and the commit + copy kernel, and launches the latter without
- * programmatic dependent launch, so that a caller can time the two kernels
- * separately with its own events.  NULL restores the default.  Host only. */
-int hs_set_phase_event(hs_state* st, void* event_host);
+/* Profiling (no counterpart on the pages): when `timeline_dev` is non-NULL,
+ * every later hs_swap_in (and hs_swap_in_noalloc) on this handle writes the
+ * phase times of its CTAs there, as uint64 [batch][8][8] indexed by batch
+ * row, cluster rank and word (8-byte aligned device memory; rows of ranks
+ * the call does not use are left untouched).  Words 0-6 are nanoseconds of
+ * the GPU's global timer: 0 CTA start, 1 de-duplication table cleared,
+ * 2 lookups and de-duplication done, 3 first-occurrence counts exchanged,
+ * 4 locations and miss lists written, 5 commit done (rank 0 only), 6 last
+ * warp done copying; word 7 is the cluster size.  A rejected batch row
+ * writes words 0-2 and 7 only.  NULL turns it off.  Host only. */
+int hs_set_timeline(hs_state* st, uint64_t* timeline_dev);
 
-/* Tuning: CTAs of the commit + copy kernel that copy miss rows (in addition
- * to one commit CTA per batch row).  0 restores the default (twice the SM
+/* Tuning: CTAs of hs_copy_planned.  0 restores the default (twice the SM
  * count); otherwise 1..65535.  Host only. */
 int hs_set_copy_ctas(hs_state* st, int32_t copy_ctas);
 
@@ -354,7 +362,7 @@ int hs_set_copy_ctas(hs_state* st, int32_t copy_ctas);
  *     other handles, no ordering between them) race on the array: order them.
  *   - Device status flags still go to the handle (read with hs_get_status).
  * Everything else (state, host pool, device buffer, deferred-copy and
- * phase-event settings) is the handle's, as for hs_swap_in. */
+ * timeline settings) is the handle's, as for hs_swap_in. */
 int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_dev,
                        const int32_t* seq_lens_dev, const int32_t* topk_dev, int32_t batch,
                        int32_t num_steps, int32_t layer_id, int32_t* device_locs_dev,

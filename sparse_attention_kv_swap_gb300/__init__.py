@@ -10,7 +10,7 @@ from .binding import (HsConfig, HsError, make_config, load_library,  # noqa: F40
                       hs_host_pool_bytes, hs_hash_size, hs_create_state, hs_destroy_state,
                       hs_swap_in, hs_page_table, hs_reset_requests, hs_get_status,
                       hs_export_request_state, hs_status_string, hs_version,
-                      hs_set_phase_event, hs_set_copy_ctas, hs_set_defer_copy,
+                      hs_set_timeline, hs_set_copy_ctas, hs_set_defer_copy,
                       hs_copy_planned, hs_append_rows, hs_get_stats)
 
 

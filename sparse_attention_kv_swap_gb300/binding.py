@@ -103,7 +103,7 @@ def _declare(lib) -> None:
         "hs_swap_in_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
                                               _vp, _vp, _vp, _vp]),
         "hs_append_rows": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
-        "hs_set_phase_event": (ctypes.c_int, [_vp, _vp]),
+        "hs_set_timeline": (ctypes.c_int, [_vp, _vp]),
         "hs_set_defer_copy": (ctypes.c_int, [_vp, _i32]),
         "hs_copy_planned": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
         "hs_set_copy_ctas": (ctypes.c_int, [_vp, _i32]),
@@ -443,10 +443,21 @@ def hs_get_stats(handle: StateHandle, layer_id: int, reset: bool = False, stream
     return out
 
 
-def hs_set_phase_event(handle: StateHandle, event=None) -> None:
-    """event: a torch.cuda.Event (created with enable_timing) or None."""
-    ptr = 0 if event is None else int(event.cuda_event)
-    _check(load_library().hs_set_phase_event(handle.ptr, ptr), "hs_set_phase_event")
+def hs_set_timeline(handle: StateHandle, timeline=None) -> None:
+    """timeline: a uint64-sized CUDA tensor of at least max_batch * 64
+    elements on the handle's device (the per-CTA phase stamps of later
+    swap-ins, [batch][8][8]), or None to stop recording."""
+    import torch
+    ptr = 0
+    with _on_device(handle.device):
+        if timeline is not None:
+            if not timeline.is_cuda:
+                raise ValueError("timeline must be in device memory")
+            if timeline.numel() < handle.cfg.max_batch * 64:
+                raise ValueError("timeline: need %d elements, got %d"
+                                 % (handle.cfg.max_batch * 64, timeline.numel()))
+            ptr = _dptr(timeline, torch.int64, "timeline")
+        _check(load_library().hs_set_timeline(handle.ptr, ptr), "hs_set_timeline")
 
 
 def hs_set_copy_ctas(handle: StateHandle, copy_ctas: int) -> None:

@@ -1,7 +1,7 @@
 // Host side of the C ABI declared in include/hisparse_swap.h: argument
-// validation, state and workspace layout, and the launch sequence of one
-// swap-in call (gather, then commit + copy with programmatic dependent
-// launch) on the caller's stream.
+// validation, state and workspace layout, and the launch of one swap-in call
+// (one kernel: lookup, de-duplication, locations, commit and miss-row copy)
+// on the caller's stream.
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -127,6 +127,7 @@ int hs_config_check(const hs_config* c) {
         c->max_batch <= 0)
         return HS_ERR_INVALID_ARG;
     if (c->item_size_bytes % 16 != 0) return HS_ERR_INVALID_ARG;
+    if (c->item_size_bytes > HS_MAX_ITEM_BYTES) return HS_ERR_UNSUPPORTED;
     if (c->max_batch > c->num_requests) return HS_ERR_INVALID_ARG;
     if (c->hot_buffer_size > HS_MAX_HOT_BUFFER) return HS_ERR_UNSUPPORTED;
     if (c->max_steps > HS_MAX_STEPS) return HS_ERR_UNSUPPORTED;
@@ -205,7 +206,7 @@ int hs_create_state(const hs_config* cfg, void* const* host_pool_host, void* con
         return HS_ERR_CUDA;
     }
     st->copy_ctas = 2 * st->num_sms;
-    st->phase_event = nullptr;
+    st->timeline = nullptr;
     st->defer_copy = 0;
     int pageable_ok = 0;
     cudaDeviceGetAttribute(&pageable_ok, cudaDevAttrPageableMemoryAccess, st->device);
@@ -285,13 +286,11 @@ int hs_swap_in(hs_state* st, const int32_t* req_pool_indices_dev, const int32_t*
     a.plan_src = reinterpret_cast<long long*>(miss_src_dev);
     a.plan_dst = reinterpret_cast<long long*>(miss_dst_dev);
     a.plan_count = miss_count_dev;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_gather(a, st->num_sms, s) != cudaSuccess) return HS_ERR_CUDA;
-    if (st->phase_event && cudaEventRecord(st->phase_event, s) != cudaSuccess) return HS_ERR_CUDA;
-    const int copy_ctas = st->defer_copy ? 0 : st->copy_ctas;
-    if (launch_commit_copy(a, copy_ctas, st->phase_event == nullptr, s) != cudaSuccess)
-        return HS_ERR_CUDA;
-    return HS_OK;
+    a.defer_copy = st->defer_copy;
+    a.timeline = st->timeline;
+    return launch_swapin(a, st->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HS_OK
+               : HS_ERR_CUDA;
 }
 
 int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
@@ -349,9 +348,9 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
                : HS_ERR_CUDA;
 }
 
-int hs_set_phase_event(hs_state* st, void* event_host) {
-    if (!st) return HS_ERR_INVALID_ARG;
-    st->phase_event = static_cast<cudaEvent_t>(event_host);
+int hs_set_timeline(hs_state* st, uint64_t* timeline_dev) {
+    if (!st || !null_or_aligned(timeline_dev, 8)) return HS_ERR_INVALID_ARG;
+    st->timeline = reinterpret_cast<unsigned long long*>(timeline_dev);
     return HS_OK;
 }
 
@@ -478,6 +477,6 @@ const char* hs_status_string(int code) {
     }
 }
 
-int32_t hs_version(void) { return 10100; }
+int32_t hs_version(void) { return 20000; }
 
 }  // extern "C"

@@ -13,7 +13,7 @@
 //     totals uint64 [layers][16]          running sums of the HS_STAT_* counters
 //   workspace (one call at a time, shared by all layers):
 //     miss_tok / miss_last / miss_dst / vict / adm  int32 [B_max][C]
-//     cnt   int32 [B_max][16]             per-request call counters
+//     cnt   int32 [B_max][16]             per-batch-row words (copy claim counter)
 //     status uint32                       sticky device status flags
 #pragma once
 
@@ -42,13 +42,12 @@ enum Ctrl : int {
 constexpr int kTotalsWords = 16;  // per layer; the first HS_NUM_STATS are used
 constexpr int kCntWords = 16;
 enum Cnt : int {
-    CNT_U = 0,        // unique misses
-    CNT_HITS = 1,     // hit entries
-    CNT_MISSES = 2,   // miss entries (unique + duplicates)
-    CNT_INVALID = 3,  // invalid entries
-    CNT_SKIP = 4,     // 1 if this batch row was rejected on the device
-    CNT_Q = 5,        // request slot of this batch row
+    CNT_CLAIM = 0,  // 16-byte pieces of the batch row's miss rows claimed by copying warps
 };
+
+// Words of the optional per-CTA timeline (hs_set_timeline): [b][rank][8].
+constexpr int kTimelineCtas = 8;   // cluster ranks per batch row (P <= 8)
+constexpr int kTimelineWords = 8;  // words per CTA
 
 struct Dims {
     int32_t R, L, W, H, K, S_max, C, layers, B_max;
@@ -93,8 +92,11 @@ struct SwapArgs {
     long long* plan_src;  // [B][C] or null
     long long* plan_dst;  // [B][C] or null
     int32_t* plan_count;  // [B] or null
-    int32_t dedup_size;   // gather's shared-memory dedup table entries (power of two)
-    int32_t dedup_shift;  // 32 - log2(dedup_size)
+    int32_t defer_copy;   // 1: record the plan only, copy no rows
+    unsigned long long* timeline;  // [B][kTimelineCtas][kTimelineWords] or null
+    // set by the launcher:
+    int32_t dedup_entries;  // entries of one CTA's share of the miss de-duplication table
+    int32_t dedup_shift;    // hash de-duplication: 32 - log2(P * dedup_entries)
 };
 
 // Byte offsets of the state and workspace regions (256-byte aligned).
@@ -143,12 +145,19 @@ cudaError_t ensure_smem(F* kernel, size_t bytes, SmemOptIn* opt) {
     return e;
 }
 
+// Launch shape of one swap-in call (see swapin_shape in hs_swapin.cu).
+struct SwapinShape {
+    int P;          // CTAs per batch row (thread-block cluster size), power of two <= 8
+    int rmax;       // entries per thread (1, 2 or 4)
+    int block;      // threads per CTA
+    bool by_position;  // miss de-duplication table indexed by token position (else hashed)
+    int dedup_entries; // entries of one CTA's share of that table
+    size_t smem;    // dynamic shared memory per CTA
+};
+SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms);
+
 // Launchers (each returns the launch's error code).
-int gather_cluster_size(int batch, int entries, int sms);
-size_t gather_smem_bytes(int entries, int cluster, int* dedup_size);
-cudaError_t launch_gather(const SwapArgs& a, int sms, cudaStream_t s);
-size_t commit_smem_bytes(const Dims& d);
-cudaError_t launch_commit_copy(const SwapArgs& a, int copy_ctas, bool pdl, cudaStream_t s);
+cudaError_t launch_swapin(const SwapArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_planned_copy(const long long* src, const long long* dst, const int32_t* count,
                                 int32_t B, int32_t C, int32_t W, const uint8_t* pool,
                                 long long pool_rows, uint8_t* kv, long long kv_rows,
@@ -182,11 +191,35 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// Programmatic dependent launch controls (sm_90 and later).
-__device__ __forceinline__ void pdl_trigger() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+// Nanoseconds of the GPU's global timer (timeline stamps).
+__device__ __forceinline__ unsigned long long global_timer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 16-byte load that bypasses L1 (each host row is read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, const uint4& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Non-binding prefetch into L2 of the 128-byte lines of [p, p + bytes) that
+// fall to this thread when `nthreads` threads numbered `first` on share them.
+__device__ __forceinline__ void l2_prefetch(const void* p, size_t bytes, int first, int nthreads) {
+    const char* c = static_cast<const char*>(p);
+    for (size_t off = (size_t)first * 128; off < bytes; off += (size_t)nthreads * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
+}
 
 // Inclusive warp scan.
 __device__ __forceinline__ int warp_inclusive_scan(int x) {
@@ -244,8 +277,8 @@ struct hs_state {
     std::vector<uint8_t*> device_kv;
     int device;
     int num_sms;
-    int copy_ctas;
-    cudaEvent_t phase_event;  // profiling split between the two kernels, or null
+    int copy_ctas;            // CTAs of hs_copy_planned
+    unsigned long long* timeline;  // per-CTA phase stamps of later calls, or null
     int defer_copy;           // 1: hs_swap_in records the miss plan but copies nothing
 };
 

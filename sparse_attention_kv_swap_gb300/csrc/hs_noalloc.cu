@@ -112,11 +112,9 @@ extern "C" int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_
     a.plan_src = reinterpret_cast<long long*>(miss_src_dev);
     a.plan_dst = reinterpret_cast<long long*>(miss_dst_dev);
     a.plan_count = miss_count_dev;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_gather(a, st->num_sms, s) != cudaSuccess) return HS_ERR_CUDA;
-    if (st->phase_event && cudaEventRecord(st->phase_event, s) != cudaSuccess) return HS_ERR_CUDA;
-    const int copy_ctas = st->defer_copy ? 0 : st->copy_ctas;
-    if (launch_commit_copy(a, copy_ctas, st->phase_event == nullptr, s) != cudaSuccess)
-        return HS_ERR_CUDA;
-    return HS_OK;
+    a.defer_copy = st->defer_copy;
+    a.timeline = st->timeline;
+    return launch_swapin(a, st->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HS_OK
+               : HS_ERR_CUDA;
 }

@@ -1,0 +1,936 @@
+// Swap-in kernel of the decode KV swap-in (sm_103a): one launch per
+// layer-call does the lookup, the miss de-duplication, the locations, the
+// policy commit and the miss-row copy.
+//
+// A thread-block cluster of P CTAs serves one batch row b (request
+// q = req_pool_indices[b]).  Its S x K top-k entries form one working set
+// (the multi-step swap report "[HiSparse] Support hisparse multi-step swap io
+// kernel", section 实现拆解 item 1: the gather flattens [batch, steps, top_k],
+// looks tokens up in the hot cache's token -> slot index and de-duplicates
+// misses across steps; the commit updates CLOCK state, rotates scratch and
+// hot locations and updates the index).  CTA rank c owns the c-th contiguous
+// slice of the flattened entries; entry (s, k) has flat index i = s * K + k.
+//   1. each thread loads up to RMAX entries; an entry on the request's extra
+//      page (its newest, still-filling page, the first lookup the same
+//      report lists) is served from its extra row; the others probe the
+//      request's token -> slot index (dense map: one load; hash bank: linear
+//      probing with every first probe issued before any resolves);
+//   2. misses go into a de-duplication table spread over the cluster's
+//      shared memory, which keeps for each token the smallest flat index at
+//      which it occurs and the set of steps it occurs in.  When the table
+//      fits, it is indexed by the token's position (home CTA t mod P, entry
+//      t / P) and an insert is two fire-and-forget atomics; otherwise it is
+//      a hash table with linear probing (compare-and-swap inserts);
+//   3. an entry is the first occurrence of its token iff the table holds its
+//      own flat index.  Each CTA turns its first-occurrence flags into a
+//      bitmap over its entries with a running count per 32-entry word, and
+//      sends its total to every CTA of the cluster;
+//   4. the ordinal j of a miss is the number of first occurrences before
+//      its token's first occurrence: the totals of lower-ranked CTAs plus
+//      that CTA's running count and bitmap up to it.  Every entry gets its
+//      device row (q * (H + C) + phys[slot] for a hit, q * (H + C) +
+//      phys[H + j] for miss j, R * (H + C) + q * E + t mod E on the extra
+//      page); hit slots take the call's epoch; first occurrences list their
+//      token, last step and device row;
+//   5. the leader CTA (rank 0) commits the request's policy state on up to
+//      512 of its threads (epoch-CLOCK victims, admission, rotation, index
+//      update), while every other warp of the cluster copies the request's
+//      miss rows from the mapped pinned host pool, claiming 16-byte pieces
+//      from a per-batch-row counter; the commit's warps join the copy when
+//      they are done.
+// A request's copy thus starts as soon as its own lookup is complete; no
+// CTA waits for another batch row.  The commit rewrites only policy state,
+// the copy only device KV rows, so the two never touch the same memory.
+#include <cooperative_groups.h>
+
+#include "hs_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace hs {
+namespace {
+
+constexpr int kMaxCluster = 8;
+constexpr int kMissPending = -2;    // code of an entry that missed the index
+constexpr int kNoFirst = 0x7fffffff;  // de-duplication entry not yet seen
+constexpr int kCopyUnroll = 6;
+constexpr int kWarpPieces = 32 * kCopyUnroll;  // 16-byte pieces a warp claims at once
+constexpr int kCommitWarps = 16;               // the leader CTA's commit warps (at most)
+constexpr unsigned kHitKey = 0xffffffffu;      // radix key of a slot referenced by the call
+// Shared memory one CTA may spend on its share of a position-indexed
+// de-duplication table (5 bytes a position); longer sequences use the
+// hashed table.
+constexpr int kPositionTableBytes = 160 * 1024;
+
+// Entry codes: >= 0 hit slot; -1 invalid; kMissPending; after step 2
+// <= -3 a miss in the de-duplication table at entry (u * 8 + home); after
+// step 3 <= -3 a miss whose token first occurs at flat index (-3 - code).
+__device__ __forceinline__ int miss_code(int x) { return -3 - x; }
+__device__ __forceinline__ int miss_value(int code) { return -3 - code; }
+
+// Warps [0, n / 32) of the CTA, synchronising on named barrier 1 (the
+// leader CTA's commit warps, while its other warps copy).
+struct Group {
+    int tid, n;
+    __device__ void sync() const { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
+};
+
+// Exclusive scan of one int per group thread; returns the prefix and the
+// group total.  `tmp` needs 33 ints of shared memory.
+__device__ int group_exclusive_scan(const Group& g, int x, int* tmp, int* total) {
+    const int lane = g.tid & 31, warp = g.tid >> 5, nwarps = g.n >> 5;
+    const int inc = warp_inclusive_scan(x);
+    if (lane == 31) tmp[warp] = inc;
+    g.sync();
+    if (warp == 0) {
+        const int w = lane < nwarps ? tmp[lane] : 0;
+        const int wi = warp_inclusive_scan(w);
+        tmp[lane] = wi - w;
+        if (lane == 31) tmp[32] = wi;
+    }
+    g.sync();
+    const int r = tmp[warp] + inc - x;
+    *total = tmp[32];
+    g.sync();
+    return r;
+}
+
+__device__ int group_sum(const Group& g, int x, int* tmp) {
+    int total;
+    group_exclusive_scan(g, x, tmp, &total);
+    return total;
+}
+
+// Hashed de-duplication: inserts token t (flat index i, step bits `steps`)
+// into its home CTA's share (already mapped into this CTA's view) starting
+// at `start`; returns the entry.  The whole table has at least twice as
+// many entries as the request has entries, so a free one always exists.
+__device__ __forceinline__ int dedup_insert(int* keys, int* first, unsigned* smask, int size,
+                                            unsigned start, int t, int i, unsigned steps,
+                                            uint32_t* status) {
+    const unsigned mask = (unsigned)size - 1u;
+    unsigned p = start;
+    for (int n = 0; n < size; ++n) {
+        const int k = atomicCAS(&keys[p], -1, t);
+        if (k == -1 || k == t) {
+            atomicMin(&first[p], i);
+            atomicOr(&smask[p >> 2], steps << ((p & 3u) * 8u));
+            return (int)p;
+        }
+        p = (p + 1u) & mask;
+    }
+    atomicOr(status, HS_STATUS_TABLE_FULL);
+    return -1;
+}
+
+// ---- commit (policy state of one request) -----------------------------------
+
+// Deletes token t from a request's hash bank (the entry must exist).
+__device__ void bank_delete(long long* bank, int shift, unsigned mask, int32_t t,
+                            uint32_t* status) {
+    unsigned p = hash_token(t, shift);
+    for (unsigned n = 0; n <= mask; ++n) {
+        const long long x = bank[p];
+        if (x == kEmpty) break;
+        if (x >= 0 && (int)(x >> 32) == t) {
+            bank[p] = kDeleted;
+            return;
+        }
+        p = (p + 1u) & mask;
+    }
+    atomicOr(status, HS_STATUS_PROBE_LIMIT);
+}
+
+// Inserts (t, slot) at the first empty or deleted entry of t's probe
+// sequence; returns 1 if the entry was never used before.
+__device__ int bank_insert(long long* bank, int shift, unsigned mask, int32_t t, int32_t slot,
+                           uint32_t* status) {
+    const long long e = make_entry(t, slot);
+    unsigned p = hash_token(t, shift);
+    for (unsigned n = 0; n <= mask; ++n) {
+        long long x = bank[p];
+        while (x < 0) {
+            const long long y = atomicCAS(reinterpret_cast<unsigned long long*>(&bank[p]),
+                                          (unsigned long long)x, (unsigned long long)e);
+            if (y == x) return x == kEmpty ? 1 : 0;
+            x = y;
+        }
+        p = (p + 1u) & mask;
+    }
+    atomicOr(status, HS_STATUS_TABLE_FULL);
+    return 0;
+}
+
+// Finds the `need`-th smallest key (1-based) among keys[0..n) that are not
+// kHitKey, by most-significant-digit radix select over `bits` bits.
+// Returns the key; *need_out is how many keys equal to it to take.
+__device__ unsigned radix_select(const Group& g, const unsigned* keys, int n, int need, int bits,
+                                 int* hist, int* sh, int* need_out) {
+    unsigned prefix = 0u;
+    const int top = ((bits + 7) / 8) * 8;
+    for (int shift = top - 8; shift >= 0; shift -= 8) {
+        for (int i = g.tid; i < 256; i += g.n) hist[i] = 0;
+        g.sync();
+        for (int v = g.tid; v < n; v += g.n) {
+            const unsigned k = keys[v];
+            if (k == kHitKey) continue;
+            if (shift + 8 < 32 && (k >> (shift + 8)) != prefix) continue;
+            atomicAdd(&hist[(k >> shift) & 255u], 1);
+        }
+        g.sync();
+        if (g.tid < 32) {
+            const int lane = g.tid;
+            int c[8];
+            int sum = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                c[k] = hist[lane * 8 + k];
+                sum += c[k];
+            }
+            const int inc = warp_inclusive_scan(sum);
+            const int exc = inc - sum;
+            if (exc < need && need <= inc) {
+                int run = exc;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (run < need && need <= run + c[k]) {
+                        sh[0] = lane * 8 + k;
+                        sh[1] = need - run;
+                    }
+                    run += c[k];
+                }
+            }
+        }
+        g.sync();
+        prefix = (prefix << 8) | (unsigned)sh[0];
+        need = sh[1];
+        g.sync();
+    }
+    *need_out = need;
+    return prefix;
+}
+
+// Commit of batch row b (request q, epoch E, U unique misses) by group g
+// (section 实现拆解 item 1 of the multi-step swap report; overflow admission
+// prefers the latest step: section 风险与影响):
+//   - hot slots referenced by the call already carry epoch E (step 4 stamped
+//     them), so cap = H - #{ep == E} and m = min(U, cap);
+//   - victims: the m non-hit slots with the smallest (epoch, slot); a radix
+//     select over epoch + 1 finds the threshold epoch and how many slots at
+//     the threshold to take (the lowest ones);
+//   - admitted misses: all if U <= cap, otherwise the m best by (last step
+//     descending, ordinal ascending);
+//   - the i-th admitted miss (ascending ordinal) takes the i-th victim
+//     (ascending slot): its old token leaves the index, phys[v] and
+//     phys[H + j] swap (the copied row becomes the hot row, no second copy),
+//     the new token enters the index and the slot takes epoch E.
+// `keys` is H words of shared memory.
+__device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, int U, int E,
+                               unsigned* keys) {
+    __shared__ int s_tmp[33];
+    __shared__ int s_hist[256];
+    __shared__ int s_sel[2];
+    __shared__ int s_misc[8];
+
+    const Dims& d = a.d;
+    const int tid = g.tid, BD = g.n;
+    const int H = d.H;
+    int32_t* ctrl = a.lv.ctrl + (long long)q * kCtrlWords;
+    int32_t* ep = a.lv.ep + (long long)q * H;
+    int32_t* tok = a.lv.tok + (long long)q * H;
+    int32_t* phys = a.lv.phys + (long long)q * (H + d.C);
+    long long* bank = a.lv.bank + (long long)q * d.hash_size;
+    const unsigned hmask = (unsigned)d.hash_size - 1u;
+    const long long wbase = (long long)b * d.C;
+    int32_t* vict = a.ws.vict + wbase;
+    int32_t* adm = a.ws.adm + wbase;
+
+    // Keys for victim selection: epoch + 1 (0 = never used), or kHitKey.
+    int nhit = 0;
+    for (int v = tid; v < H; v += BD) {
+        const int e = ep[v];
+        const bool hit = (e == E);
+        keys[v] = hit ? kHitKey : (unsigned)(e + 1);
+        nhit += hit;
+    }
+    nhit = group_sum(g, nhit, s_tmp);  // includes the barrier that publishes keys
+    const int cap = H - nhit;
+    const int m = U < cap ? U : cap;
+
+    int evicted = 0;
+    if (m > 0) {
+        // ---- victims: m smallest (key, slot) among non-hit slots ------------
+        const int bits = 32 - __clz(E);  // keys lie in [0, E]
+        int need = m;
+        unsigned thr = 0u;
+        if (bits > 0) thr = radix_select(g, keys, H, m, bits, s_hist, s_sel, &need);
+        // Each warp owns a contiguous chunk of slots, read lane by lane, so
+        // ballots keep ascending slot order without shared-memory conflicts.
+        const int lane = tid & 31, warp = tid >> 5, nw = BD >> 5;
+        const int chunk = ((H + nw - 1) / nw + 31) & ~31;
+        const int w0 = warp * chunk, w1 = min(H, w0 + chunk);
+        int eq = 0;
+        for (int v0 = w0; v0 < w1; v0 += 32) {
+            const int v = v0 + lane;
+            eq += __popc(__ballot_sync(0xffffffffu, v < w1 && keys[v] == thr));
+        }
+        int eq_total;
+        const int eq_before = group_exclusive_scan(g, lane == 0 ? eq : 0, s_tmp, &eq_total);
+        const int eq_w = __shfl_sync(0xffffffffu, eq_before, 0);
+        int nv = 0;
+        {
+            int er = eq_w;
+            for (int v0 = w0; v0 < w1; v0 += 32) {
+                const int v = v0 + lane;
+                const unsigned k = v < w1 ? keys[v] : kHitKey;
+                const unsigned em = __ballot_sync(0xffffffffu, k == thr);
+                const bool take = k < thr || (k == thr && er + __popc(em & lanemask_lt()) < need);
+                nv += __popc(__ballot_sync(0xffffffffu, take));
+                er += __popc(em);
+            }
+        }
+        int nv_total;
+        const int v_before = group_exclusive_scan(g, lane == 0 ? nv : 0, s_tmp, &nv_total);
+        {
+            int er = eq_w;
+            int vpos = __shfl_sync(0xffffffffu, v_before, 0);
+            for (int v0 = w0; v0 < w1; v0 += 32) {
+                const int v = v0 + lane;
+                const unsigned k = v < w1 ? keys[v] : kHitKey;
+                const unsigned em = __ballot_sync(0xffffffffu, k == thr);
+                const bool take = k < thr || (k == thr && er + __popc(em & lanemask_lt()) < need);
+                const unsigned tm = __ballot_sync(0xffffffffu, take);
+                if (take) vict[vpos + __popc(tm & lanemask_lt())] = v;
+                vpos += __popc(tm);
+                er += __popc(em);
+            }
+        }
+        // ---- admitted misses ---------------------------------------------------
+        if (U > cap) {
+            const int* last = a.ws.miss_last + wbase;
+            if (tid < 8) s_misc[tid] = 0;
+            g.sync();
+            for (int x0 = tid & ~31; x0 < U; x0 += BD) {  // per-step counts, one add per warp
+                const int j = x0 + lane;
+                const int l = j < U ? last[j] : -1;
+                for (int st = 0; st < a.S; ++st) {
+                    const int c = __popc(__ballot_sync(0xffffffffu, l == st));
+                    if (lane == 0 && c) atomicAdd(&s_misc[st], c);
+                }
+            }
+            g.sync();
+            // threshold step: walk from the latest step down
+            int s_thr = 0, need_s = m, acc = 0;
+            for (int s = a.S - 1; s >= 0; --s) {
+                if (acc + s_misc[s] >= m) {
+                    s_thr = s;
+                    need_s = m - acc;
+                    break;
+                }
+                acc += s_misc[s];
+            }
+            const int cj = ((U + nw - 1) / nw + 31) & ~31;
+            const int j0 = warp * cj, j1 = min(U, j0 + cj);
+            int eqs = 0;
+            for (int x0 = j0; x0 < j1; x0 += 32) {
+                const int j = x0 + lane;
+                eqs += __popc(__ballot_sync(0xffffffffu, j < j1 && last[j] == s_thr));
+            }
+            int eqs_total;
+            const int es_before = group_exclusive_scan(g, lane == 0 ? eqs : 0, s_tmp, &eqs_total);
+            const int es_w = __shfl_sync(0xffffffffu, es_before, 0);
+            int na = 0;
+            {
+                int er = es_w;
+                for (int x0 = j0; x0 < j1; x0 += 32) {
+                    const int j = x0 + lane;
+                    const int l = j < j1 ? last[j] : -1;
+                    const unsigned em = __ballot_sync(0xffffffffu, l == s_thr);
+                    const bool take =
+                        l > s_thr || (l == s_thr && er + __popc(em & lanemask_lt()) < need_s);
+                    na += __popc(__ballot_sync(0xffffffffu, take));
+                    er += __popc(em);
+                }
+            }
+            int na_total;
+            const int a_before = group_exclusive_scan(g, lane == 0 ? na : 0, s_tmp, &na_total);
+            {
+                int er = es_w;
+                int apos = __shfl_sync(0xffffffffu, a_before, 0);
+                for (int x0 = j0; x0 < j1; x0 += 32) {
+                    const int j = x0 + lane;
+                    const int l = j < j1 ? last[j] : -1;
+                    const unsigned em = __ballot_sync(0xffffffffu, l == s_thr);
+                    const bool take =
+                        l > s_thr || (l == s_thr && er + __popc(em & lanemask_lt()) < need_s);
+                    const unsigned tm = __ballot_sync(0xffffffffu, take);
+                    if (take) adm[apos + __popc(tm & lanemask_lt())] = j;
+                    apos += __popc(tm);
+                    er += __popc(em);
+                }
+            }
+        }
+        g.sync();
+        // ---- evict, rotate and admit ------------------------------------------
+        // A pair's four loads are independent.  Deletions and insertions may
+        // interleave: a deletion only rewrites an entry that holds its own
+        // (live) key and an insertion only claims empty or deleted entries,
+        // so an insertion that probes past a live entry being deleted just
+        // lands further along its chain.
+        int fresh = 0;
+        const int32_t* mtok = a.ws.miss_tok + wbase;
+        for (int i = tid; i < m; i += BD) {
+            const int v = vict[i];
+            const int j = (U > cap) ? adm[i] : i;
+            const int old = tok[v];
+            const int pv = phys[v];
+            const int ps = phys[H + j];
+            const int t = mtok[j];
+            phys[v] = ps;
+            phys[H + j] = pv;
+            tok[v] = t;
+            ep[v] = E;
+            if (d.dense) {  // dense index: one store each (old != t: resident vs not)
+                int16_t* map = a.lv.map + (long long)q * d.L;
+                if (old >= 0) {
+                    map[old] = -1;
+                    ++evicted;
+                }
+                map[t] = (int16_t)v;
+                continue;
+            }
+            if (old >= 0) {
+                bank_delete(bank, d.hash_shift, hmask, old, a.ws.status);
+                ++evicted;
+            }
+            fresh += bank_insert(bank, d.hash_shift, hmask, t, v, a.ws.status);
+        }
+        evicted = group_sum(g, evicted, s_tmp);
+        fresh = group_sum(g, fresh, s_tmp);
+        if (tid == 0) {
+            s_misc[0] = ctrl[CTRL_USED] + fresh;
+            s_misc[1] = ctrl[CTRL_RESIDENT] + m - evicted;
+        }
+        g.sync();
+        // ---- rebuild the bank once deleted entries pile up ---------------------
+        if (!d.dense && s_misc[0] > (d.hash_size / 4) * 3) {
+            for (int p = tid; p < d.hash_size; p += BD) bank[p] = kEmpty;
+            g.sync();
+            for (int v = tid; v < H; v += BD) {
+                const int t = tok[v];
+                if (t >= 0) bank_insert(bank, d.hash_shift, hmask, t, v, a.ws.status);
+            }
+            if (tid == 0) {
+                s_misc[0] = s_misc[1];
+                ctrl[CTRL_REBUILDS] += 1;
+            }
+        }
+        g.sync();
+        if (tid == 0) {
+            ctrl[CTRL_USED] = s_misc[0];
+            ctrl[CTRL_RESIDENT] = s_misc[1];
+        }
+    }
+    if (tid == 0) {
+        ctrl[CTRL_EPOCH] = E + 1;
+        ctrl[CTRL_LOCK] = 0;
+        if (a.stats) {
+            int32_t* st = a.stats + (long long)b * HS_NUM_STATS;
+            st[HS_STAT_HIT_SLOTS] = nhit;
+            st[HS_STAT_ADMITTED] = m;
+            st[HS_STAT_EVICTED] = evicted;
+            st[HS_STAT_OVERFLOW] = U - m;
+        }
+        unsigned long long* tot = a.lv.totals;  // the layer's running sums
+        atomicAdd(tot + HS_STAT_HIT_SLOTS, (unsigned long long)nhit);
+        atomicAdd(tot + HS_STAT_ADMITTED, (unsigned long long)m);
+        atomicAdd(tot + HS_STAT_EVICTED, (unsigned long long)evicted);
+        atomicAdd(tot + HS_STAT_OVERFLOW, (unsigned long long)(U - m));
+    }
+}
+
+// ---- copy (miss rows of one request) -----------------------------------------
+
+// Copies the U miss rows of one request (W bytes each) from its host pool
+// rows to their device rows, one warp at a time: a warp claims kWarpPieces
+// consecutive 16-byte pieces of the flattened (miss, piece) space from
+// `claim`, issues all its loads, then its stores, and claims again until
+// the pieces run out.  `mtok` and `mdst` were written earlier in this
+// kernel, so they are read with plain (coherent) loads.
+__device__ void copy_request(const uint8_t* pool_q, uint8_t* kv, const int32_t* mtok,
+                             const int32_t* mdst, int U, int W, unsigned* claim) {
+    const int lane = threadIdx.x & 31;
+    const unsigned nv = (unsigned)W >> 4;  // 16-byte pieces per row
+    const unsigned total = (unsigned)U * nv;
+    for (;;) {
+        unsigned start = 0;
+        if (lane == 0) start = atomicAdd(claim, (unsigned)kWarpPieces);
+        start = __shfl_sync(0xffffffffu, start, 0);
+        if (start >= total) break;
+        uint4 v[kCopyUnroll];
+        long long dst[kCopyUnroll];  // destination byte offset of each piece, -1 if none
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const unsigned p = start + (unsigned)(u * 32 + lane);
+            dst[u] = -1;
+            if (p < total) {
+                const unsigned row = p / nv;
+                const unsigned piece = p - row * nv;
+                dst[u] = (long long)mdst[row] * W + ((long long)piece << 4);
+                v[u] = ld_stream_v4(pool_q + (long long)mtok[row] * W + ((long long)piece << 4));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u)
+            if (dst[u] >= 0) st_v4(kv + dst[u], v[u]);
+    }
+}
+
+// ---- the kernel ----------------------------------------------------------------
+
+template <int RMAX, bool BY_POSITION>
+__global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_ok, s_epoch, s_done;
+    __shared__ int s_tot[kMaxCluster];
+    __shared__ int s_cnt[4];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int P = (int)cluster.num_blocks();
+    const int c = (int)cluster.block_rank();
+    const int plog = __ffs(P) - 1;
+
+    const Dims& d = a.d;
+    const int b = blockIdx.x >> plog;  // clusters are P consecutive CTAs
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int BD = blockDim.x, nwarps = BD >> 5;
+    const int N = a.S * d.K;
+    const int per = (N + P - 1) / P;
+    const int lo = c * per, hi = min(N, lo + per);
+    unsigned long long* tl =
+        a.timeline ? a.timeline + ((long long)b * kTimelineCtas + c) * kTimelineWords : nullptr;
+    if (tl && tid == 0) {
+        tl[0] = global_timer();
+        tl[7] = (unsigned long long)P;
+    }
+
+    // This CTA's share of the de-duplication table, then the bitmap words.
+    const int TS = a.dedup_entries;
+    int* first = reinterpret_cast<int*>(smem);                  // smallest flat index
+    unsigned* smask = reinterpret_cast<unsigned*>(first + TS);  // 8 step bits an entry
+    int* keys = reinterpret_cast<int*>(smask + (TS >> 2));      // hashed table: the tokens
+    const int table_bytes = ((BY_POSITION ? 5 : 9) * TS + 15) & ~15;
+    // word w = r * nwarps + warp of this CTA's entries: (running count << 32) | flags
+    unsigned long long* fw = reinterpret_cast<unsigned long long*>(smem + table_bytes);
+
+    // ---- 0. independent loads first: request slot, length, this CTA's entries
+    const int q = __ldg(a.rpi + b);
+    const int sl = __ldg(a.seq_lens + b);
+    const int32_t* topk_b = a.topk + (long long)b * N;
+    int t[RMAX], code[RMAX], aux[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+        const int i = lo + r * BD + tid;
+        t[r] = (i < hi) ? __ldg(topk_b + i) : -1;
+    }
+    const bool q_ok = q >= 0 && q < d.R;
+    const int limit = sl < d.L ? sl : d.L;
+    // first position of the extra page (past every valid token if none)
+    const int xstart = (d.E > 0 && limit > 0) ? (limit - 1) / d.E * d.E : 0x7fffffff;
+    unsigned xbits = 0u;  // bit r: entry r is on the extra page
+    const long long base = (long long)q * (d.H + d.C);
+    const int32_t* phys = a.lv.phys + base;
+    if (q_ok) {
+        // Warm L2 for later steps: the scratch positions (locations of the
+        // misses, step 4) and the epochs (the commit).
+        l2_prefetch(phys + d.H, (size_t)d.C * 4, c * BD + tid, P * BD);
+        if (c == 0) l2_prefetch(a.lv.ep + (long long)q * d.H, (size_t)d.H * 4, tid, BD);
+    }
+    {
+        int4* f4 = reinterpret_cast<int4*>(first);
+        for (int x = tid; x < (TS >> 2); x += BD) f4[x] = make_int4(kNoFirst, kNoFirst, kNoFirst, kNoFirst);
+        int4* m4 = reinterpret_cast<int4*>(smask);
+        for (int x = tid; x < (TS >> 4); x += BD) m4[x] = make_int4(0, 0, 0, 0);
+        if (!BY_POSITION) {
+            int4* k4 = reinterpret_cast<int4*>(keys);
+            for (int x = tid; x < (TS >> 2); x += BD) k4[x] = make_int4(-1, -1, -1, -1);
+        }
+    }
+    unsigned* claim = reinterpret_cast<unsigned*>(a.ws.cnt + (long long)b * kCntWords + CNT_CLAIM);
+    if (c == 0 && tid == 0) *claim = 0u;
+    if (tid < 4) s_cnt[tid] = 0;
+    if (tid == 0) s_done = 0;
+    cluster.sync();  // every CTA of the cluster runs and its table share is empty
+    if (tl && tid == 0) tl[1] = global_timer();
+
+    // ---- 1. probe the token -> slot index ------------------------------------
+    {
+        const long long* bank = a.lv.bank + (long long)(q_ok ? q : 0) * d.hash_size;
+        const unsigned hmask = (unsigned)d.hash_size - 1u;
+        const int16_t* map = a.lv.map + (long long)(q_ok ? q : 0) * d.L;
+        long long e[RMAX];
+        unsigned pos[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            const bool in_range = q_ok && (lo + r * BD + tid < hi) && t[r] >= 0 && t[r] < limit;
+            const bool extra = in_range && t[r] >= xstart;
+            const bool valid = in_range && !extra;  // goes through the index
+            if (extra) xbits |= 1u << r;
+            code[r] = valid ? kMissPending : -1;
+            e[r] = kEmpty;
+            pos[r] = 0u;
+            if (d.dense) {  // dense index: the slot is one load away, no chain
+                if (valid) {
+                    const int slot = map[t[r]];
+                    if (slot >= 0 && slot < d.H) code[r] = slot;
+                }
+                continue;
+            }
+            pos[r] = hash_token(t[r], d.hash_shift);
+            if (valid) e[r] = bank[pos[r]];
+        }
+        if (c == 0 && tid == 0) {
+            // The request lock and epoch, decided once and sent to every CTA.
+            int ok = 1;
+            if (!q_ok) {
+                atomicOr(a.ws.status, HS_STATUS_BAD_REQUEST);
+                ok = 0;
+            } else if (atomicCAS(&a.lv.ctrl[(long long)q * kCtrlWords + CTRL_LOCK], 0, 1) != 0) {
+                atomicOr(a.ws.status, HS_STATUS_DUPLICATE_REQUEST);
+                ok = 0;
+            }
+            if (sl > d.L) atomicOr(a.ws.status, HS_STATUS_SEQ_LEN_CLAMPED);
+            const int E = ok ? a.lv.ctrl[(long long)q * kCtrlWords + CTRL_EPOCH] : 0;
+            for (int r = 0; r < P; ++r) {
+                *cluster.map_shared_rank(&s_ok, r) = ok;
+                *cluster.map_shared_rank(&s_epoch, r) = E;
+            }
+        }
+        if (!d.dense) {
+#pragma unroll
+            for (int r = 0; r < RMAX; ++r) {
+                if (code[r] == -1) continue;
+                for (int n = 0;; ++n) {
+                    const long long x = e[r];
+                    if (x == kEmpty) break;  // not resident
+                    if (x >= 0 && (int)(x >> 32) == t[r]) {
+                        const int slot = (int)(x & 0xffffffffll);
+                        if (slot < d.H) code[r] = slot;
+                        else atomicOr(a.ws.status, HS_STATUS_PROBE_LIMIT);  // corrupt entry
+                        break;
+                    }
+                    if (n + 1 >= d.hash_size) {
+                        atomicOr(a.ws.status, HS_STATUS_PROBE_LIMIT);
+                        break;
+                    }
+                    pos[r] = (pos[r] + 1u) & hmask;
+                    e[r] = bank[pos[r]];
+                }
+            }
+        }
+    }
+    // Hits: fetch the slot's physical row now (the epoch stamp waits for the lock).
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) aux[r] = code[r] >= 0 ? phys[code[r]] : 0;
+
+    // ---- 2. de-duplicate misses into the cluster-wide table ------------------
+    if (BY_POSITION) {
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            if (code[r] != kMissPending) continue;
+            const int i = lo + r * BD + tid;
+            const int home = t[r] & (P - 1);
+            const int u = t[r] >> plog;
+            atomicMin(cluster.map_shared_rank(first, home) + u, i);
+            atomicOr(cluster.map_shared_rank(smask, home) + (u >> 2),
+                     (1u << (i / d.K)) << ((u & 3) * 8));
+            code[r] = miss_code(u * kMaxCluster + home);
+        }
+    } else {
+        const int ts_log = __ffs(TS) - 1;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            const int i = lo + r * BD + tid;
+            const bool miss = code[r] == kMissPending;
+            // equal tokens of one warp insert once, by their lowest lane
+            const unsigned grp = __match_any_sync(0xffffffffu, miss ? t[r] : (-2 - lane));
+            if (miss) {
+                const int leader = __ffs(grp) - 1;
+                const unsigned steps = __reduce_or_sync(grp, 1u << (i / d.K));
+                int x = -1;
+                if (lane == leader) {
+                    const unsigned h = hash_token(t[r], a.dedup_shift);
+                    const int home = (int)(h >> ts_log);
+                    const int u = dedup_insert(cluster.map_shared_rank(keys, home),
+                                               cluster.map_shared_rank(first, home),
+                                               cluster.map_shared_rank(smask, home), TS,
+                                               h & (unsigned)(TS - 1), t[r], i, steps,
+                                               a.ws.status);
+                    x = u >= 0 ? u * kMaxCluster + home : -1;
+                }
+                x = __shfl_sync(grp, x, leader);
+                code[r] = x >= 0 ? miss_code(x) : -1;
+            }
+        }
+    }
+    cluster.sync();  // the table is complete, s_ok / s_epoch have arrived
+    if (tl && tid == 0) tl[2] = global_timer();
+
+    int32_t* locs_b = a.locs + (long long)b * N;
+    if (!s_ok) {
+        // Rejected batch row: no location, no state change, nothing to copy.
+        for (int i = lo + tid; i < hi; i += BD) locs_b[i] = -1;
+        if (c == 0) {
+            if (a.stats && tid < HS_NUM_STATS) a.stats[(long long)b * HS_NUM_STATS + tid] = 0;
+            if (a.plan_count && tid == 0) a.plan_count[b] = 0;
+        }
+        return;
+    }
+    const int E = s_epoch;
+    {
+        int32_t* ep = a.lv.ep + (long long)q * d.H;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+            if (code[r] >= 0) ep[code[r]] = E;  // hit slots take the call's epoch
+    }
+
+    // ---- 3. first occurrences: flags, running counts, totals -----------------
+    {
+        unsigned mw[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {  // all remote loads in flight together
+            mw[r] = 0u;
+            if (code[r] <= -3) {
+                const int x = miss_value(code[r]);
+                const int home = x & (kMaxCluster - 1), u = x >> 3;
+                aux[r] = *(cluster.map_shared_rank(first, home) + u);
+                mw[r] = *(cluster.map_shared_rank(smask, home) + (u >> 2));
+                mw[r] = (mw[r] >> ((u & 3) * 8)) & 0xffu;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            const int i = lo + r * BD + tid;
+            const bool f = code[r] <= -3 && aux[r] == i;
+            if (code[r] <= -3) {
+                code[r] = miss_code(aux[r]);     // now: first index of the token
+                aux[r] = 31 - __clz((int)mw[r]);  // last step in which it occurs
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, f);
+            if (lane == 0) fw[r * nwarps + warp] = bal;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // running counts over the RMAX * nwarps words in (r, warp) order
+        const int n = RMAX * nwarps;
+        const int per_lane = (n + 31) >> 5;
+        unsigned bw[RMAX];
+        int sum = 0;
+#pragma unroll
+        for (int k = 0; k < RMAX; ++k) {
+            const int idx = lane * per_lane + k;
+            bw[k] = (k < per_lane && idx < n) ? (unsigned)fw[idx] : 0u;
+            sum += __popc(bw[k]);
+        }
+        const int inc = warp_inclusive_scan(sum);
+        int run = inc - sum;
+#pragma unroll
+        for (int k = 0; k < RMAX; ++k) {
+            const int idx = lane * per_lane + k;
+            if (k < per_lane && idx < n) {
+                fw[idx] = ((unsigned long long)(unsigned)run << 32) | bw[k];
+                run += __popc(bw[k]);
+            }
+        }
+        const int total = __shfl_sync(0xffffffffu, inc, 31);
+        if (lane < P) *cluster.map_shared_rank(&s_tot[c], lane) = total;
+    }
+    cluster.sync();  // every CTA's words and total are in place
+    if (tl && tid == 0) tl[3] = global_timer();
+
+    // ---- 4. ordinals, locations, miss lists, counters -----------------------
+    int U = 0;
+    for (int k = 0; k < P; ++k) U += s_tot[k];
+    const long long wbase = (long long)b * d.C;
+    {
+        int j[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {  // remote words of other CTAs' first occurrences
+            j[r] = 0;
+            if (code[r] <= -3) {
+                const int i1 = miss_value(code[r]);
+                const int c1 = i1 / per;
+                const int l1 = i1 - c1 * per;
+                const unsigned long long wd = c1 == c
+                                                  ? fw[l1 >> 5]
+                                                  : *(cluster.map_shared_rank(fw, c1) + (l1 >> 5));
+                int off = 0;
+                for (int k = 0; k < c1; ++k) off += s_tot[k];
+                j[r] = off + (int)(wd >> 32) +
+                       __popc((unsigned)wd & ((1u << (l1 & 31)) - 1u));
+            }
+        }
+        int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            const int i = lo + r * BD + tid;
+            if (i >= hi) continue;
+            int loc;
+            if ((xbits >> r) & 1u) {
+                loc = (int)((long long)d.R * (d.H + d.C) + (long long)q * d.E + t[r] % d.E);
+                ++n_ext;
+            } else if (code[r] >= 0) {
+                loc = (int)(base + aux[r]);
+                ++n_hit;
+            } else if (code[r] == -1) {
+                loc = -1;
+                ++n_inv;
+            } else {
+                loc = (int)(base + phys[d.H + j[r]]);
+                ++n_miss;
+                if (miss_value(code[r]) == i) {  // first occurrence: list the miss
+                    a.ws.miss_tok[wbase + j[r]] = t[r];
+                    a.ws.miss_last[wbase + j[r]] = aux[r];
+                    a.ws.miss_dst[wbase + j[r]] = loc;
+                    if (a.plan_src) {
+                        a.plan_src[wbase + j[r]] = (long long)q * d.L + t[r];
+                        a.plan_dst[wbase + j[r]] = loc;
+                    }
+                }
+            }
+            locs_b[i] = loc;
+        }
+        n_hit = __reduce_add_sync(0xffffffffu, n_hit);
+        n_inv = __reduce_add_sync(0xffffffffu, n_inv);
+        n_miss = __reduce_add_sync(0xffffffffu, n_miss);
+        n_ext = __reduce_add_sync(0xffffffffu, n_ext);
+        if (lane == 0) {
+            int* rc = cluster.map_shared_rank(s_cnt, 0);
+            atomicAdd(&rc[0], n_hit);
+            atomicAdd(&rc[1], n_inv);
+            atomicAdd(&rc[2], n_miss);
+            if (n_ext) atomicAdd(&rc[3], n_ext);
+        }
+    }
+    // Counters complete, miss lists and epoch stamps visible to the whole
+    // cluster; no shared memory of another CTA is touched after this point.
+    cluster.sync();
+    if (tl && tid == 0) tl[4] = global_timer();
+    if (c == 0 && tid == 0) {
+        const int n_hit = s_cnt[0], n_inv = s_cnt[1], n_miss = s_cnt[2];
+        if (a.stats) {
+            int32_t* st = a.stats + (long long)b * HS_NUM_STATS;
+            st[HS_STAT_HITS] = n_hit;
+            st[HS_STAT_DUP_MISSES] = n_miss - U;
+            st[HS_STAT_UNIQUE_MISSES] = U;
+            st[HS_STAT_INVALID] = n_inv;
+            st[HS_STAT_EXTRA] = s_cnt[3];
+        }
+        unsigned long long* tot = a.lv.totals;  // the layer's running sums
+        atomicAdd(tot + HS_STAT_HITS, (unsigned long long)n_hit);
+        atomicAdd(tot + HS_STAT_DUP_MISSES, (unsigned long long)(n_miss - U));
+        atomicAdd(tot + HS_STAT_UNIQUE_MISSES, (unsigned long long)U);
+        atomicAdd(tot + HS_STAT_INVALID, (unsigned long long)n_inv);
+        atomicAdd(tot + HS_STAT_EXTRA, (unsigned long long)s_cnt[3]);
+        if (a.plan_count) a.plan_count[b] = U;
+    }
+
+    // ---- 5. commit on the leader's first warps, copy everywhere else --------
+    const int commit_warps = nwarps < kCommitWarps ? nwarps : kCommitWarps;
+    if (c == 0 && warp < commit_warps) {
+        commit_request(a, Group{tid, commit_warps * 32}, b, q, U, E,
+                       reinterpret_cast<unsigned*>(smem));
+        if (tl && tid == 0) tl[5] = global_timer();
+    }
+    if (!a.defer_copy && U > 0)
+        copy_request(a.lv.host_pool + (long long)q * d.L * d.W, a.lv.device_kv,
+                     a.ws.miss_tok + wbase, a.ws.miss_dst + wbase, U, d.W, claim);
+    if (tl && lane == 0 && atomicAdd(&s_done, 1) == nwarps - 1) tl[6] = global_timer();
+}
+
+template <int RMAX, bool BY_POSITION>
+cudaError_t launch_one(const SwapArgs& a, const SwapinShape& sh, cudaStream_t s) {
+    static SmemOptIn opt_in;
+    cudaError_t e = ensure_smem(swapin_kernel<RMAX, BY_POSITION>, sh.smem, &opt_in);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.B * sh.P);
+    cfg.blockDim = dim3(sh.block);
+    cfg.dynamicSmemBytes = sh.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = sh.P;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, swapin_kernel<RMAX, BY_POSITION>, a);
+}
+
+}  // namespace
+
+// Launch shape of a call with `batch` rows of `steps * K` entries:
+//   - P, the CTAs per batch row: the largest power of two <= 8 with
+//     batch * P CTAs still within one wave of `sms` SMs and at least 256
+//     entries per CTA, but never more than 4096 entries per CTA (4 a
+//     thread); then raised (up to 8) until a position-indexed
+//     de-duplication table over max_seq_len positions fits
+//     kPositionTableBytes per CTA.  If it never fits, the table is hashed.
+//   - threads: 1024 for more than 1024 entries per CTA, else the entries
+//     rounded up to whole warps, at least 256 (512 with H >= 2048, since
+//     the leader CTA's threads also run the commit over the H slots).
+//   - shared memory: the table share plus the bitmap words, or the commit's
+//     H keys if larger.
+SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
+    const int N = steps * d.K;
+    int p = 1;
+    while (p < kMaxCluster && batch * (2 * p) <= sms && N / (2 * p) >= 256) p *= 2;
+    while (p < kMaxCluster && (N + p - 1) / p > 4096) p *= 2;
+    auto pos_entries = [&](int pp) { return ((d.L + pp - 1) / pp + 15) & ~15; };
+    int pp = p;
+    while (pp < kMaxCluster && 5 * pos_entries(pp) > kPositionTableBytes) pp *= 2;
+    SwapinShape sh;
+    sh.by_position = 5 * pos_entries(pp) <= kPositionTableBytes;
+    if (sh.by_position) p = pp;
+    sh.P = p;
+    if (sh.by_position) {
+        sh.dedup_entries = pos_entries(p);
+    } else {
+        int t1 = 128;
+        while (t1 < 2 * N) t1 <<= 1;
+        sh.dedup_entries = t1 / p;
+    }
+    const int per = (N + p - 1) / p;
+    const int min_block = d.H >= 2048 ? 512 : 256;
+    if (per <= 1024) {
+        sh.rmax = 1;
+        const int w = ((per + 31) / 32) * 32;
+        sh.block = w < min_block ? min_block : w;
+    } else {
+        sh.rmax = per <= 2048 ? 2 : 4;
+        sh.block = 1024;
+    }
+    const size_t table = (size_t)(((sh.by_position ? 5 : 9) * sh.dedup_entries + 15) & ~15);
+    const size_t words = (size_t)sh.rmax * (sh.block / 32) * 8;
+    const size_t commit = (size_t)d.H * 4;
+    sh.smem = table + words > commit ? table + words : commit;
+    return sh;
+}
+
+cudaError_t launch_swapin(const SwapArgs& a, int sms, cudaStream_t s) {
+    const SwapinShape sh = swapin_shape(a.d, a.B, a.S, sms);
+    SwapArgs g = a;
+    g.dedup_entries = sh.dedup_entries;
+    g.dedup_shift = 32 - __builtin_ctz((unsigned)(sh.dedup_entries * sh.P));
+    if (sh.by_position) {
+        if (sh.rmax == 1) return launch_one<1, true>(g, sh, s);
+        if (sh.rmax == 2) return launch_one<2, true>(g, sh, s);
+        return launch_one<4, true>(g, sh, s);
+    }
+    if (sh.rmax == 1) return launch_one<1, false>(g, sh, s);
+    if (sh.rmax == 2) return launch_one<2, false>(g, sh, s);
+    return launch_one<4, false>(g, sh, s);
+}
+
+}  // namespace hs

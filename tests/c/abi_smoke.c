@@ -49,7 +49,7 @@ int main(void) {
     expect(hs_append_rows(NULL, 0, NULL, NULL, NULL, NULL, 1, NULL) == HS_ERR_INVALID_ARG,
            "append without a handle");
     expect(strcmp(hs_status_string(HS_OK), "ok") == 0, "status string");
-    expect(hs_version() == 10100, "version");
+    expect(hs_version() == 20000, "version");
     hs_destroy_state(NULL);
     if (failures) return 1;
     printf("ok\n");

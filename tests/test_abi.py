@@ -35,7 +35,7 @@ def test_header_constants_match_binding():
 
 
 def test_version_and_strings(lib):
-    assert pkg.hs_version() == 10100
+    assert pkg.hs_version() == 20000
     assert pkg.hs_status_string(0) == "ok"
     assert "invalid" in pkg.hs_status_string(-1)
     assert pkg.hs_status_string(-99) == "unknown status"

@@ -1,7 +1,7 @@
 """Register and stack report of every kernel, compiled for sm_103a here (no GPU
 needed).  No kernel may spill registers or keep a stack frame, and the
-kernels whose launch bounds promise full occupancy (the gather at 1024
-threads per SM, the commit + copy and planned-copy kernels at 2 x 512) must
+kernels whose launch bounds promise full occupancy (the swap-in kernel at
+1024 threads per SM, the planned-copy kernel at 2 x 512) must
 fit 64 registers a thread, so that the bounds hold without spilling.  A change
 that breaks either shows up here before it costs time on the GPU.  The same
 sources, and the CPU oracle, also compile with warnings as errors."""
@@ -15,7 +15,7 @@ import pytest
 
 from sparse_attention_kv_swap_gb300 import build
 
-FULL_OCCUPANCY = ("gather_kernel", "commit_copy_kernel", "planned_copy_kernel")
+FULL_OCCUPANCY = ("swapin_kernel", "planned_copy_kernel")
 EXPECTED = FULL_OCCUPANCY + ("append_kernel", "page_table_kernel", "reset_kernel")
 
 
