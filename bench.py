@@ -1,9 +1,11 @@
 """Benchmark of the per-layer decode KV swap-in on one GB300 (or N replicas).
 
-One step is one layer-call of the whole hot path on one batch: gather
-(hash probe, cross-step miss dedup, locations), then commit (epoch-CLOCK
-victims, rotation, hash update) side by side with the miss-row copy from the
-pinned host pool, plus the sparse page table for the paged workload.
+One step is one layer-call of the whole hot path on one batch, in one kernel:
+lookup (token -> slot index), cross-step miss de-duplication and locations,
+then the commit (epoch-CLOCK victims, rotation, index update) side by side
+with the miss-row copy from the pinned host pool; plus the sparse page table
+for the paged workload.  The default workload is the largest configuration,
+the 4-step (MTP) swap at batch 64 (C3).
 
 Metric: selected tokens resolved per second per layer-call (B * S * K / step
 time).  Inputs (top-k, request slots, sequence lengths) are resident on the
@@ -13,7 +15,7 @@ steps.  Each timed step is bracketed by CUDA events on the launching stream.
 per step the host->device copy of the inputs from pinned memory and the
 device->host read of the locations are inside the timed region.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C2]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C3]
                        [--impl reference]
 Under torchrun each rank drives one GPU with its own copy of the workload
 (replicas, weak scaling); rank 0 prints one JSON line.
@@ -38,23 +40,13 @@ if ROOT not in sys.path:
 import hs_workloads as W  # noqa: E402
 
 METRIC = "selected tokens resolved/s per layer-call"
-# Per-launch counters of the current kernels, from ncu captures of the timed
-# steps (steady state, after an L2 flush), per workload and index:
-#   commit_copy_kernel: syslts__t_sectors_aperture_sysmem_op_read (host-link
-#   reads, 32 B sectors) and dram__bytes_read + write; gather_kernel: DRAM bytes.
-# Combinations without a capture report their traffic as null.
-NCU_TRAFFIC = {("C2", "dense"): {"commit_copy_host_link_bytes": 348905 * 32,
-                                 "commit_copy_dram_bytes": 3965696 + 26880,
-                                 "gather_dram_bytes": 5014101},
-               ("C3", "dense"): {"commit_copy_host_link_bytes": 1299617 * 32,
-                                 "commit_copy_dram_bytes": 9947562 + 2838528,
-                                 "gather_dram_bytes": 8358229},
-               ("C4", "dense"): {"commit_copy_host_link_bytes": 689289 * 32,
-                                 "commit_copy_dram_bytes": 934485 + 16469,
-                                 "gather_dram_bytes": 1382485},
-               ("C5", "dense"): {"commit_copy_host_link_bytes": 53057 * 32,
-                                 "commit_copy_dram_bytes": 1794048 + 170,
-                                 "gather_dram_bytes": 1046101}}
+# Per-launch counters of the swap-in kernel from one ncu capture per
+# workload of the timed steps (steady state, after an L2 flush), recorded in
+# profiles/swapin_kernel_traffic.md: DRAM read + write bytes and host-link
+# (system memory) read bytes.  Workloads without a capture of the current
+# kernel report null.
+NCU_TRAFFIC = {}
+NCU_CAPTURE = "profiles/swapin_kernel_traffic.md"
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
 # Untimed steps run right after each gate, before the timed ones.  On GB300
@@ -72,7 +64,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="C2", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--config", default="C3", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--copy-ctas", type=int, default=0)
     ap.add_argument("--index", default="dense", choices=["hash", "dense"],
@@ -288,9 +280,10 @@ def run_reference(args, w):
 
 def copy_ceiling(torch, pkg, cache, w, dev, flush, rows_per_request, reps=10):
     """Host-link ceiling of the library's row copy: replays synthetic miss
-    plans with hs_copy_planned (same kernel code as the swap-in's copy) for
+    plans with hs_copy_planned (16-byte vector copies like the swap-in's) for
     (a) consecutive host rows and (b) random host rows, the latter with as many
-    rows per request as a measured step.  Writes device rows, so it runs after
+    rows per request as a measured step, in random and in ascending order and
+    at 128-byte aligned offsets.  Writes device rows, so it runs after
     every other measurement."""
     Bn, C, H, L, Wr = w.batch, w.steps * w.top_k, w.hot_buffer, w.seq_len, w.row_bytes
     rng = np.random.default_rng(5)
@@ -299,7 +292,7 @@ def copy_ceiling(torch, pkg, cache, w, dev, flush, rows_per_request, reps=10):
     # rows whose host byte offset is a multiple of 128 (t * W % 128 == 0)
     align = 128 // int(np.gcd(Wr, 128))
     for kind, n in (("consecutive_rows", C), ("random_rows", n_step),
-                    ("random_rows_128B_aligned", n_step)):
+                    ("random_rows_ascending", n_step), ("random_rows_128B_aligned", n_step)):
         n = min(n, C)
         src = np.zeros((Bn, C), np.int64)
         dst = np.zeros((Bn, C), np.int64)
@@ -308,6 +301,8 @@ def copy_ceiling(torch, pkg, cache, w, dev, flush, rows_per_request, reps=10):
                 toks = np.arange(n) + rng.integers(0, L - n + 1)
             elif kind == "random_rows":
                 toks = rng.choice(L, size=n, replace=False)
+            elif kind == "random_rows_ascending":  # the same kind of rows in host order
+                toks = np.sort(rng.choice(L, size=n, replace=False))
             else:
                 n = min(n, L // align)
                 toks = rng.choice(L // align, size=n, replace=False) * align
@@ -486,46 +481,76 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
     return out
 
 
-def run_compare_sequential(args, w):
-    """Multi-step swap (one S-step call) against sequential per-step swap (S
-    single-step calls) on the same index stream, each captured as a CUDA
-    graph, as in the multi-step swap report's benchmark (section 实现拆解
-    item 4; its 48.2% figure is for batch 64, 4 steps on an H20)."""
-    import torch
-    import sparse_attention_kv_swap_gb300 as pkg
+def phase_times(tls):
+    """Phase spans of each timed launch from the kernel's timeline stamps.
+
+    tls: int64 [launches, batch, 8 ranks, 8 words] as written with
+    hs_set_timeline (words 0-6 global-timer ns, word 7 the cluster size).
+    Per launch, with t0 the first CTA's start:
+      gather_span   = last word 4 (locations and miss lists written) - t0;
+      commit_span   = last word 5 of the leader CTAs - their first word 4;
+      commit        = each leader CTA's word 5 - word 4;
+      copy_span     = last word 6 (a CTA's last warp done) - first word 4.
+    The summary gives, in microseconds from t0, the median over launches of
+    the median and the last CTA at each stamp."""
+    tls = np.asarray(tls, dtype=np.int64)
+    names = ("table_cleared", "dedup_done", "counts_exchanged", "lists_written",
+             "commit_done", "copy_done")
+    out = {"gather_span_us": [], "commit_span_us": [], "commit_us": [], "copy_span_us": []}
+    marks = {n: ([], []) for n in names}
+    for t in tls:
+        P = int(t[0, 0, 7])
+        used = t[:, :P, :]
+        t0 = used[:, :, 0].min()
+        out["gather_span_us"].append((used[:, :, 4].max() - t0) / 1e3)
+        lead = t[:, 0, :]
+        out["commit_span_us"].append((lead[:, 5].max() - lead[:, 4].min()) / 1e3)
+        out["commit_us"].extend(((lead[:, 5] - lead[:, 4]) / 1e3).tolist())
+        out["copy_span_us"].append((used[:, :, 6].max() - used[:, :, 4].min()) / 1e3)
+        for k, n in enumerate(names, start=1):
+            v = (lead[:, 5] if n == "commit_done" else used[:, :, k].ravel()) - t0
+            marks[n][0].append(float(np.median(v)) / 1e3)
+            marks[n][1].append(float(v.max()) / 1e3)
+    out["summary"] = {n: {"median_cta": statistics.median(m[0]), "last_cta": statistics.median(m[1])}
+                      for n, m in marks.items()}
+    out["summary"]["cluster_size"] = int(tls[0, 0, 0, 7])
+    return out
+
+
+def multi_vs_sequential(torch, pkg, w, dev, flush, calls, pool, dense, n=20, warmup=5):
+    """F1: the multi-step swap (one S-step call) against sequential per-step
+    swap (S single-step calls) on the same index stream, each captured as a
+    CUDA graph and replayed after an L2 flush, as in the multi-step swap
+    report's benchmark (section 实现拆解 item 4; its 48.2% figure is for
+    batch 64, 4 steps on an H20).  Two fresh caches on the same host pool,
+    with the bench's index kind."""
     from sparse_attention_kv_swap_gb300.cache import SwapInCache
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    K, Wm = args.steps, args.warmup
-    calls = W.TopkStream(w).calls(PREROLL_CALLS + Wm + K)
-    cfg = pkg.make_config(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, 1)
-    pool = torch.empty((w.batch, w.seq_len, w.row_bytes), dtype=torch.uint8, pin_memory=True)
-    W.fill_host_pool(pool.numpy(), 0)
+    Bn, S, Kk = w.batch, w.steps, w.top_k
+    cfg = pkg.make_config(Bn, w.seq_len, w.row_bytes, w.hot_buffer, Kk, S, 1,
+                          index_kind=1 if dense else 0)
     multi = SwapInCache(cfg, host_pools=[pool], device=dev)
     seq = SwapInCache(cfg, host_pools=[pool], device=dev)
     rpi = torch.from_numpy(W.req_pool_indices(w)).to(dev)
     sl = torch.from_numpy(W.seq_lens(w)).to(dev)
-    Bn, S, Kk = w.batch, w.steps, w.top_k
     buf_m = torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)
     buf_s = [torch.empty((Bn, 1, Kk), dtype=torch.int32, device=dev) for _ in range(S)]
     out_m = {"device_locs": torch.empty((Bn, S, Kk), dtype=torch.int32, device=dev)}
     out_s = [{"device_locs": torch.empty((Bn, 1, Kk), dtype=torch.int32, device=dev)}
              for _ in range(S)]
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream()
+    stream = torch.cuda.Stream(device=dev)
 
     def load(c):
         t = torch.from_numpy(c).to(dev)
         buf_m.copy_(t)
-        for s in range(S):
-            buf_s[s].copy_(t[:, s:s + 1])
+        for k in range(S):
+            buf_s[k].copy_(t[:, k:k + 1])
 
     def run_multi():
         multi.swap_in(rpi, sl, buf_m, 0, out=out_m, stream=stream)
 
     def run_seq():
-        for s in range(S):
-            seq.swap_in(rpi, sl, buf_s[s], 0, out=out_s[s], stream=stream)
+        for k in range(S):
+            seq.swap_in(rpi, sl, buf_s[k], 0, out=out_s[k], stream=stream)
 
     load(calls[0])
     torch.cuda.synchronize()
@@ -542,10 +567,10 @@ def run_compare_sequential(args, w):
         run_seq()
     torch.cuda.synchronize()
     t_m, t_s = [], []
-    for i, c in enumerate(calls):
+    for i, c in enumerate(calls[:PREROLL_CALLS + warmup + n]):
         load(c)
         torch.cuda.synchronize()
-        timed = i >= PREROLL_CALLS + Wm
+        timed = i >= PREROLL_CALLS + warmup
         for g, acc in ((g_multi, t_m), (g_seq, t_s)):
             flush.fill_(i & 0xFF)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -563,16 +588,41 @@ def run_compare_sequential(args, w):
     for cache in (multi, seq):
         rc, flags = cache.status()
         if flags:
-            raise RuntimeError("device status flags %#x" % flags)
-    ms_m, ms_s = statistics.mean(t_m), statistics.mean(t_s)
-    line = {"metric": "multi-step vs sequential per-step swap latency reduction",
-            "value": 1.0 - ms_m / ms_s, "unit": "fraction", "higher_is_better": True,
-            "multi_step_ms": ms_m, "sequential_ms": ms_s,
+            raise RuntimeError("device status flags %#x in the multi-step comparison" % flags)
+        cache.close()
+    # medians: a single slow replay (seen on a shared box) would move a mean
+    ms_m, ms_s = statistics.median(t_m), statistics.median(t_s)
+    return {"latency_reduction": 1.0 - ms_m / ms_s, "multi_step_ms": ms_m,
+            "sequential_ms": ms_s, "multi_step_ms_mean": statistics.mean(t_m),
+            "sequential_ms_mean": statistics.mean(t_s),
             "multi_step_tokens_per_s": w.entries / (ms_m * 1e-3),
-            "sequential_tokens_per_s": w.entries / (ms_s * 1e-3),
-            "steps": K, "warmup": Wm, "cuda_graph": True, "data": "synthetic",
-            "config": config_dict(w, 1),
+            "sequential_tokens_per_s": w.entries / (ms_s * 1e-3), "steps": n,
+            "index": "dense" if dense else "hash", "cuda_graph": True,
             "context": "pages: 48.2% at batch 64, 4 steps, H20 (Hopper)"}
+
+
+def run_compare_sequential(args, w):
+    """--compare-sequential: F1 alone, as its own JSON line."""
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    calls = W.TopkStream(w).calls(PREROLL_CALLS + args.warmup + args.steps)
+    pool = torch.empty((w.batch, w.seq_len, w.row_bytes), dtype=torch.uint8, pin_memory=True)
+    W.fill_host_pool(pool.numpy(), 0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    clocks.wait_first()
+    t0 = time.time()
+    f1 = multi_vs_sequential(torch, pkg, w, dev, flush, calls, pool, args.index == "dense",
+                             n=args.steps, warmup=args.warmup)
+    t1 = time.time()
+    clocks.stop()
+    line = {"metric": "multi-step vs sequential per-step swap latency reduction",
+            "value": f1["latency_reduction"], "unit": "fraction", "higher_is_better": True,
+            **f1, "warmup": args.warmup, "data": "synthetic", "config": config_dict(w, 1),
+            "clocks": clocks.summary(t0, t1)}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -726,8 +776,6 @@ def main():
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    time.sleep(0.05)
-    clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = max_over_ranks(torch, sum(step_ms) / K, world, dev)
     value = whole_job_rate(w.entries, world, ms)
@@ -738,29 +786,32 @@ def main():
     ev_alt = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n_alt)]
 
-    # ---- phase split: gather vs commit + copy (separate pass, same stream) ----
+    # ---- phase split from the kernel's own timeline (separate pass) ----
+    # Every CTA stamps the GPU's global timer at its phase boundaries
+    # (hs_set_timeline); the launches are direct, each between two events.
+    tl = torch.zeros((Bn, 8, 8), dtype=torch.int64, device=dev)
+    tls = torch.zeros((n_phase, Bn, 8, 8), dtype=torch.int64, device=dev)
     e_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
-    e_m = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
     e_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
-    for e in e_m:  # torch creates the CUDA event at its first record
-        e.record(s)
     pbase = base + K + PRIMER_STEPS
+    pkg.hs_set_timeline(cache.handle, tl)
+    torch.cuda.synchronize()
     gate(torch, n_phase + PRIMER_STEPS)
     for i in range(base + K, pbase):
         flush.fill_(i & 0xFF)
         step(i, topk_all[i])
     for k in range(n_phase):
         flush.fill_(k & 0xFF)
-        pkg.hs_set_phase_event(cache.handle, e_m[k])
         e_a[k].record(s)
         cache.swap_in(rpi, sl, topk_all[pbase + k], 0,
                       out={"device_locs": locs, "stats": stats[pbase + k]})
         e_b[k].record(s)
-    pkg.hs_set_phase_event(cache.handle, None)
+        tls[k].copy_(tl)
     torch.cuda.synchronize()
-    t_gather = [a.elapsed_time(m) for a, m in zip(e_a, e_m)]
-    t_cc = [m.elapsed_time(b) for m, b in zip(e_m, e_b)]
+    pkg.hs_set_timeline(cache.handle, None)
+    t_kernel = [a.elapsed_time(b) for a, b in zip(e_a, e_b)]
     st_phase = stats[pbase:pbase + n_phase].cpu().numpy()
+    timeline = phase_times(tls.cpu().numpy())
 
     # ---- e2e: host buffers through the same C ABI call ----
     # Each step's inputs sit in one pinned host record [top-k | slots | lengths]
@@ -866,28 +917,50 @@ def main():
     pipeline = deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool,
                                       args.index == "dense", n=min(K, 10))
 
+    f1_t0 = time.time()
+    f1 = multi_vs_sequential(torch, pkg, w, dev, flush, calls, pool, args.index == "dense",
+                             n=min(K, 20), warmup=Wm)
+    f1_t1 = time.time()
+    clocks.stop()
+    f1["clocks"] = clocks.summary(f1_t0, f1_t1)
+
     # ---- roofline bookkeeping (algorithmic bytes) ----
+    U_timed = st_timed[:, :, 3].sum(axis=1).astype(np.float64)
+    copy_bytes_timed = U_timed * w.row_bytes  # host-link bytes (same again written to HBM)
+    achieved_copy = float(np.mean(copy_bytes_timed) / (np.mean(step_ms) * 1e-3) / 1e9)
     U_phase = st_phase[:, :, 3].sum(axis=1).astype(np.float64)
     m_phase = st_phase[:, :, 4].sum(axis=1).astype(np.float64)
     hs_phase = st_phase[:, :, 1].sum(axis=1).astype(np.float64)
-    copy_bytes = U_phase * w.row_bytes  # host-link bytes (same again written to HBM)
-    cc_ms = np.asarray(t_cc)
-    g_ms = np.asarray(t_gather)
-    achieved_copy = float(np.mean(copy_bytes / (cc_ms * 1e-3)) / 1e9)
     gather_bytes = 16.0 * w.entries + 16.0 * U_phase
     commit_bytes = 8.0 * w.hot_buffer * w.batch + 32.0 * m_phase + 4.0 * hs_phase
-    achieved_gather = float(np.mean(gather_bytes / (g_ms * 1e-3)) / 1e9)
-    U_timed = st_timed[:, :, 3].sum(axis=1)
+    copy_bytes_phase = U_phase * w.row_bytes
 
+    def hbm_phase(nbytes, span_us):
+        achieved = float(np.mean(nbytes / (np.asarray(span_us) * 1e-6)) / 1e9)
+        return {"achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_source": hbm_src,
+                "algorithmic_bytes_per_launch": float(np.mean(nbytes)),
+                "span_us_mean": float(np.mean(span_us))}
+
+    traffic = NCU_TRAFFIC.get((args.config, args.index), {})
+    gather_hbm = dict(hbm_phase(gather_bytes, timeline["gather_span_us"]),
+                      span="first CTA start to the last CTA's locations and miss lists",
+                      traffic=traffic.get("gather_dram_bytes"))
+    commit_hbm = dict(hbm_phase(commit_bytes, timeline["commit_span_us"]),
+                      span="first leader CTA's commit start to the last one's end "
+                           "(each request's commit starts when its own lookup ends)",
+                      per_request_commit_us_median=float(np.median(timeline["commit_us"])))
+    copy_window = copy_bytes_phase / (np.asarray(timeline["copy_span_us"]) * 1e-6) / 1e9
     clk = clocks.summary(t_wall0, t_wall1)
-    n_kernels = 2 + (1 if page_out is not None else 0)
+    n_kernels = 1 + (1 if page_out is not None else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": dict(config_dict(w, world), index=args.index, launch=(
-            "one CUDA graph per step (gather + commit/copy), replayed; the step's top-k is "
+            "one CUDA graph per step (the swap-in kernel%s), replayed; the step's top-k is "
             "staged into the graph's input buffer before the step's events"
+            % (" and, on a second stream, the page table" if page_out is not None else "")
             if args.launch == "graph" else "direct launches through the C ABI")),
         "e2e": {"value": whole_job_rate(w.entries, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h_bytes),
@@ -899,27 +972,30 @@ def main():
                                      "the call; the kernels read and write them over "
                                      "NVLink-C2C (no copy-engine transfer)"}},
         "gpu_launches": K * n_kernels,
-        "roofline": {"kernel": "commit_copy_kernel (commit CTAs + miss-row copy CTAs)",
+        "roofline": {"kernel": "swapin_kernel (lookup, de-duplication, locations, commit and "
+                               "miss-row copy in one launch)",
                      "bound": "host_link", "achieved": achieved_copy, "peak": h2d_peak,
                      "unit": "GB/s", "frac": achieved_copy / h2d_peak,
-                     "traffic": NCU_TRAFFIC.get((args.config, args.index), {}).get("commit_copy_dram_bytes"),
-                     "host_link_traffic": NCU_TRAFFIC.get((args.config, args.index), {}).get(
-                         "commit_copy_host_link_bytes"),
-                     "traffic_note": "traffic = DRAM read+write bytes per launch (the commit's "
-                                     "state rows); host_link_traffic = system-memory read "
-                                     "bytes per launch, the link this kernel is bound by; both "
-                                     "from one ncu capture of this workload",
+                     "traffic": traffic.get("dram_bytes"),
+                     "host_link_traffic": traffic.get("host_link_bytes"),
+                     "traffic_note": ("traffic = DRAM read+write bytes per launch; "
+                                      "host_link_traffic = system-memory read bytes per "
+                                      "launch, the link this kernel is bound by; both from "
+                                      "the ncu capture of this workload in " + NCU_CAPTURE)
+                     if traffic else "no ncu capture of the current kernel on this workload",
                      "peak_source": "measured in this run: pinned host->device cudaMemcpyAsync "
                                     "256 MiB, best of 20",
-                     "algorithmic_bytes_per_launch": float(np.mean(copy_bytes))},
+                     "algorithmic_bytes_per_launch": float(np.mean(copy_bytes_timed)),
+                     "duration": "mean event-timed step of the timed region (one launch "
+                                 "of this kernel per step)"},
         "phases": {
-            "gather_ms": float(np.mean(g_ms)), "commit_copy_ms": float(np.mean(cc_ms)),
-            "gather_hbm": {"achieved": achieved_gather, "peak": hbm_peak, "unit": "GB/s",
-                           "frac": achieved_gather / hbm_peak, "peak_source": hbm_src,
-                           "algorithmic_bytes_per_launch": float(np.mean(gather_bytes)),
-                           "traffic": NCU_TRAFFIC.get((args.config, args.index), {}).get(
-                               "gather_dram_bytes")},
-            "commit_bytes_per_launch": float(np.mean(commit_bytes)),
+            "kernel_ms_direct": float(np.mean(t_kernel)),
+            "timeline_us": timeline["summary"],
+            "gather_hbm": gather_hbm,
+            "commit_hbm": commit_hbm,
+            "copy_window": {"gbs": float(np.mean(copy_window)), "peak": h2d_peak,
+                            "frac": float(np.mean(copy_window)) / h2d_peak,
+                            "span": "first lookup end to the last warp's copy end"},
             "unique_misses_per_step": float(np.mean(U_timed)),
             "miss_copy_mb_per_step": float(np.mean(U_timed)) * w.row_bytes / 1e6,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
@@ -933,6 +1009,7 @@ def main():
                                       "when they fit the hot buffer (an overflowing "
                                       "workload still misses: see unique_misses_per_step)"},
         },
+        "multi_vs_sequential": f1,
         "copy_ceiling": ceiling,
         "decode_step_extra_page": decode,
         "deferred_copy_pipeline": pipeline,

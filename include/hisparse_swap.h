@@ -153,11 +153,19 @@ typedef struct hs_config {
 typedef struct hs_state hs_state; /* opaque host handle */
 
 /* Returns HS_OK if `cfg` is valid and supported, else the error code.
- * Host only; no CUDA call. */
+ * Host only; no CUDA call.  The limits are the multi-step swap report's
+ * (section 风险与影响: hot_buffer_size up to 32768; 实现拆解 item 2: up to 4
+ * speculative steps) and this build's (HS_MAX_*). */
 int hs_config_check(const hs_config* cfg);
 
 /* Sizes the caller must allocate (0 if the config is not accepted).
- * Host only; no CUDA call.
+ * Host only; no CUDA call.  The state holds what the multi-step swap
+ * report's HiSparseSpecState holds (section 关键源码片段: the per-request
+ * hash banks of cache_index, the reference epochs of cache_policy, the
+ * reusable scratch locations and counters of scratch_locs / scratch_state),
+ * in this library's layout; the host pool is the pinned pool that PR #20343
+ * maps between device and host (PR #20343 summary, 实现拆解: the memory
+ * pool extended with a device-host mapping).
  *   state:      device bytes, persistent cache state of all layers
  *               (hash banks, slot epochs, slot tokens, position table,
  *               control words)
@@ -173,7 +181,10 @@ size_t hs_host_pool_bytes(const hs_config* cfg);
 int32_t hs_hash_size(const hs_config* cfg);
 
 /* Creates the host handle and initialises the state on `stream`: every
- * request empty, no token resident, position table the identity, epoch 0.
+ * request empty, no token resident, position table the identity, epoch 0
+ * (the persistent state of HiSparseSpecState, multi-step swap report,
+ * section 关键源码片段; the pages do not state an initial value, and this
+ * library reads it as an empty cache).
  *   host_pool_host[l]: host pool of layer l, 16-byte aligned.  Pinned memory
  *     (cudaHostAlloc'd or cudaHostRegister'ed) is used through its device
  *     mapping (cudaHostGetDevicePointer).  Plain pageable memory is accepted
@@ -191,7 +202,9 @@ int hs_create_state(const hs_config* cfg, void* const* host_pool_host,
                     void* workspace_dev, size_t workspace_bytes, void* stream,
                     hs_state** out);
 
-/* Frees the host handle only (never the caller's memory). NULL is a no-op. */
+/* Frees the host handle only (never the caller's memory). NULL is a no-op.
+ * (Lifetime of the handle of hs_create_state; no counterpart on the pages,
+ * whose state object is a Python tuple of tensors.) */
 void hs_destroy_state(hs_state* st);
 
 /* One per-layer swap-in call (the page's swap_in_selected_pages(
@@ -262,7 +275,10 @@ int hs_append_rows(hs_state* st, int32_t layer_id, const int32_t* req_dev,
 
 /* Returns requests to the empty state in every layer (use when a request
  * slot is given to a new sequence; order it after the previous user's last
- * call and before the new user's first call on `stream`).  Only policy
+ * call and before the new user's first call on `stream`: the PR #20343
+ * summary, sections 评论区精华 and 风险与影响, reports an illegal-address
+ * crash when admitting a request into staging was not ordered by a stream
+ * wait under overlapped scheduling).  Only policy
  * state is reset: KV rows (host pool, device buffer, extra page) are left as
  * they are, and the new sequence's rows arrive through its own prefill and
  * hs_append_rows. */
@@ -271,10 +287,15 @@ int hs_reset_requests(hs_state* st, const int32_t* req_pool_indices_dev, int32_t
 
 /* Synchronises `stream`, returns the device status flags (HS_STATUS_*) in
  * *flags_out and clears them.  Returns HS_ERR_DEVICE_STATUS if any flag was
- * set, HS_OK otherwise. */
+ * set, HS_OK otherwise.  (No counterpart on the pages: the kernels record
+ * out-of-range request slots, duplicate requests and probe limits here
+ * instead of touching memory out of bounds, the kind of fault the PR #20343
+ * summary, section 评论区精华, reports as cudaErrorIllegalAddress.) */
 int hs_get_status(hs_state* st, uint32_t* flags_out, void* stream);
 
 /* Running sums of the per-request counters (HS_STAT_*) of layer `layer_id`
+ * (the pages count a call's unique cross-step misses in their test: the
+ * multi-step swap report, section 实现拆解 item 4, 782 unique misses)
  * over every swap-in call since the handle was created or last read with
  * `reset` (a monitoring aid: hit rate, misses, evictions, overflow).  Rows
  * rejected on the device add nothing.  Copies HS_NUM_STATS int64 values to
@@ -284,7 +305,9 @@ int hs_get_stats(hs_state* st, int32_t layer_id, int64_t* totals_host, int32_t r
                  void* stream);
 
 /* Copies one request's policy state of one layer to host memory and
- * synchronises `stream` (checkpointing and tests).  Any output may be NULL.
+ * synchronises `stream` (checkpointing and tests; the state is that of
+ * HiSparseSpecState, multi-step swap report, section 关键源码片段, in this
+ * library's layout).  Any output may be NULL.
  *   tok_host  int32 [H]: token held by each hot slot, -1 if empty
  *   ep_host   int32 [H]: epoch of the slot's last reference, -1 if never
  *   phys_host int32 [H + C]: physical row of each position (a permutation)
@@ -332,7 +355,9 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
 int hs_set_timeline(hs_state* st, uint64_t* timeline_dev);
 
 /* Tuning: CTAs of hs_copy_planned.  0 restores the default (twice the SM
- * count); otherwise 1..65535.  Host only. */
+ * count); otherwise 1..65535.  Host only.  (The pages flag a hard-coded
+ * launch shape as a risk on other hardware: PR #20343 summary, 风险与影响,
+ * block_size=256; this keeps the replay's grid a parameter.) */
 int hs_set_copy_ctas(hs_state* st, int32_t copy_ctas);
 
 /* Size of the per-call scratch array of hs_swap_in_noalloc (16 MiB). */
@@ -343,23 +368,27 @@ int hs_set_copy_ctas(hs_state* st, int32_t copy_ctas);
  *
  * Some callers cannot call cudaMalloc, or any routine that allocates, on the
  * path that issues swap-ins.  Examples: a plugin that a serving runtime hands
- * only its input and output tensors, and code that must not allocate while a
- * stream is being captured.  This call takes the same arguments as
- * hs_swap_in and gives the same results.  Its per-call scratch (miss lists,
- * victim and admission lists, per-request counters) lives in one file-scope
- * device array of HS_NOALLOC_SCRATCH_BYTES, not in the handle's workspace.
- * Every GPU that loads the library holds that array until the process exits.
- * The call allocates nothing.
- *   - A call needs 5 * align256(4 * batch * C) + align256(64 * batch) bytes
+ * only its input and output tensors, and a runtime whose device memory all
+ * comes from its own pool, reserved up front, where an allocation behind its
+ * back could fail or fragment that pool.  This call takes the same arguments
+ * as hs_swap_in and gives the same results.  Its per-call scratch (miss
+ * lists, admission list, per-batch-row words) lives in one
+ * file-scope device array of HS_NOALLOC_SCRATCH_BYTES, not in the handle's
+ * workspace.  Every GPU that loads the library holds that array until the
+ * process exits.  The call allocates nothing.
+ *   - A call needs 4 * align256(4 * batch * C) + align256(64 * batch) bytes
  *     (C = max_steps * top_k).  A larger call returns HS_ERR_UNSUPPORTED
- *     before any launch; e.g. batch 64 with C = 8192 needs 10.5 MB.
+ *     before any launch; e.g. batch 64 with C = 8192 needs 8.4 MB.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current.  Make that first
- *     call before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and so does the first
+ *     call after the device's context was created again (for example after
+ *     cudaDeviceReset): an address is kept per device and context.  Make
+ *     that first call before any stream capture.
  *   - All calls share the array, and it keeps the last call's contents.
- *     Nothing in it needs clearing: a call writes every element before it
- *     reads it.  Calls whose kernels can overlap on the GPU (other streams,
- *     other handles, no ordering between them) race on the array: order them.
+ *     Nothing in it needs clearing: a call zeroes the words it counts with
+ *     and writes every list entry before it reads it.  Calls whose kernels
+ *     can overlap on the GPU (other streams, other handles, no ordering
+ *     between them) race on the array: order them.
  *   - Device status flags still go to the handle (read with hs_get_status).
  * Everything else (state, host pool, device buffer, deferred-copy and
  * timeline settings) is the handle's, as for hs_swap_in. */
@@ -369,10 +398,11 @@ int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_dev,
                        int32_t* stats_dev, int64_t* miss_src_dev, int64_t* miss_dst_dev,
                        int32_t* miss_count_dev, void* stream);
 
-/* Static string for a return code. */
+/* Static string for a return code (no counterpart on the pages). */
 const char* hs_status_string(int code);
 
-/* Library ABI version (major * 10000 + minor * 100 + patch). */
+/* Library ABI version (major * 10000 + minor * 100 + patch; no counterpart
+ * on the pages). */
 int32_t hs_version(void);
 
 #ifdef __cplusplus

@@ -41,6 +41,8 @@ HS_NUM_STATS = 9
 STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "evicted",
               "overflow", "invalid", "extra")
 HS_MAX_EXTRA_PAGE = 65536
+HS_MAX_ITEM_BYTES = 65536
+HS_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 HEADER = os.path.join(_build.INCLUDE, "hisparse_swap.h")
 

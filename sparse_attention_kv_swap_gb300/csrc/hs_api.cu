@@ -69,8 +69,6 @@ WorkspaceLayout workspace_layout(const Dims& d) {
     o = align256(o + bc);
     w.miss_dst = o;
     o = align256(o + bc);
-    w.vict = o;
-    o = align256(o + bc);
     w.adm = o;
     o = align256(o + bc);
     w.cnt = o;
@@ -105,7 +103,6 @@ Workspace workspace_view(const Dims& d, uint8_t* ws) {
     v.miss_tok = reinterpret_cast<int32_t*>(ws + w.miss_tok);
     v.miss_last = reinterpret_cast<int32_t*>(ws + w.miss_last);
     v.miss_dst = reinterpret_cast<int32_t*>(ws + w.miss_dst);
-    v.vict = reinterpret_cast<int32_t*>(ws + w.vict);
     v.adm = reinterpret_cast<int32_t*>(ws + w.adm);
     v.cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
     v.status = reinterpret_cast<uint32_t*>(ws + w.status);

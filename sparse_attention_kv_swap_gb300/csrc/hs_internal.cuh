@@ -12,7 +12,7 @@
 //     ctrl  int32 [layers][R][8]          control words (see Ctrl)
 //     totals uint64 [layers][16]          running sums of the HS_STAT_* counters
 //   workspace (one call at a time, shared by all layers):
-//     miss_tok / miss_last / miss_dst / vict / adm  int32 [B_max][C]
+//     miss_tok / miss_last / miss_dst / adm  int32 [B_max][C]
 //     cnt   int32 [B_max][16]             per-batch-row words (copy claim counter)
 //     status uint32                       sticky device status flags
 #pragma once
@@ -73,7 +73,6 @@ struct Workspace {
     int32_t* miss_tok;   // [B_max][C] token of unique miss j
     int32_t* miss_last;  // [B_max][C] last step in which miss j occurs
     int32_t* miss_dst;   // [B_max][C] device row miss j was written to
-    int32_t* vict;       // [B_max][C] victims in ascending slot order
     int32_t* adm;        // [B_max][C] admitted ordinals in ascending order
     int32_t* cnt;        // [B_max][kCntWords]
     uint32_t* status;    // sticky HS_STATUS_* flags
@@ -104,7 +103,7 @@ struct StateLayout {
     size_t bank, map, ep, tok, phys, ctrl, totals, total;
 };
 struct WorkspaceLayout {
-    size_t miss_tok, miss_last, miss_dst, vict, adm, cnt, status, total;
+    size_t miss_tok, miss_last, miss_dst, adm, cnt, status, total;
 };
 
 StateLayout state_layout(const Dims& d);

@@ -3,12 +3,16 @@
 //
 // Some callers cannot call cudaMalloc (or any routine that allocates) on the
 // path that issues swap-ins.  Examples are a plugin that a serving runtime
-// hands only its input and output tensors, and code that must not allocate
-// while a stream is being captured.  This entry point behaves exactly like
-// hs_swap_in, but the per-call scratch of the two kernels (miss lists, victim
-// and admission lists, per-request counters) lives in one file-scope device
-// array of fixed size, not in the handle's workspace.  Every GPU that loads
-// the library holds the array until the process exits.
+// hands only its input and output tensors, and a runtime whose device memory
+// all comes from its own pool, reserved up front, so that an allocation
+// behind its back could fail or fragment that pool.  This entry point behaves
+// exactly like hs_swap_in, but the per-call scratch of the kernel (miss
+// lists, admission list, per-batch-row words) lives in one
+// file-scope device array of fixed size, not in the handle's workspace.
+// Every GPU that loads the library holds the array until the process exits.
+#include <cuda.h>  // CUcontext and CUresult only: the two driver calls below come
+                   // from the runtime's entry-point query, so nothing links libcuda
+
 #include <mutex>
 
 #include "hs_internal.cuh"
@@ -22,32 +26,79 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[HS_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddress {
+    unsigned long long context;  // id of the context the address belongs to (0: none)
+    void* addr;
+};
+ScratchAddress g_scratch[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context, or 0 if there is
+// none yet or it cannot be read.  A device's primary context gets a new id
+// when it is created again (after cudaDeviceReset, for example), and a
+// symbol's address is only valid in the context it was looked up in.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+        cudaGetLastError();  // a failed query is not sticky; clear it
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Device address of the scratch array on `device` (the current device),
-// looked up once per device.
+// Device address of the scratch array on `device` (the current device).
+// Looked up once per device and context: the first call on a device, and
+// the first after its context was created again, asks the runtime
+// (cudaGetSymbolAddress, which also makes the context current on this
+// thread if it was not); later calls reuse the address.
 cudaError_t scratch_address(int device, unsigned char** out) {
     if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[device]) {
+    unsigned long long ctx = current_context_id();
+    ScratchAddress& slot = g_scratch[device];
+    if (ctx == 0 || slot.addr == nullptr || slot.context != ctx) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[device] = p;
+        if (ctx == 0) ctx = current_context_id();  // the lookup made the context current
+        slot.context = ctx;
+        slot.addr = ctx ? p : nullptr;  // without a context id, look it up every call
+        *out = static_cast<unsigned char*>(p);
+        return cudaSuccess;
     }
-    *out = static_cast<unsigned char*>(g_scratch_addr[device]);
+    *out = static_cast<unsigned char*>(slot.addr);
     return cudaSuccess;
 }
 
 }  // namespace
 
 // Bytes of per-call scratch a call with `batch` rows needs (same regions as
-// the handle's workspace, sized for `batch` rather than max_batch).
+// the handle's workspace, sized for `batch` rather than max_batch).  The
+// kernel zeroes the per-batch-row words it counts with before using them,
+// and writes every list entry before reading it, so nothing needs clearing.
 static size_t noalloc_bytes(const Dims& d, int batch) {
     const size_t bc = align256((size_t)batch * d.C * 4);
-    return 5 * bc + align256((size_t)batch * kCntWords * 4);
+    return 4 * bc + align256((size_t)batch * kCntWords * 4);
 }
 
 }  // namespace hs
@@ -92,9 +143,8 @@ extern "C" int hs_swap_in_noalloc(hs_state* st, const int32_t* req_pool_indices_
     ws.miss_tok = reinterpret_cast<int32_t*>(scratch);
     ws.miss_last = reinterpret_cast<int32_t*>(scratch + bc);
     ws.miss_dst = reinterpret_cast<int32_t*>(scratch + 2 * bc);
-    ws.vict = reinterpret_cast<int32_t*>(scratch + 3 * bc);
-    ws.adm = reinterpret_cast<int32_t*>(scratch + 4 * bc);
-    ws.cnt = reinterpret_cast<int32_t*>(scratch + 5 * bc);
+    ws.adm = reinterpret_cast<int32_t*>(scratch + 3 * bc);
+    ws.cnt = reinterpret_cast<int32_t*>(scratch + 4 * bc);
     ws.status = reinterpret_cast<uint32_t*>(st->ws + st->wl.status);
 
     SwapArgs a = {};

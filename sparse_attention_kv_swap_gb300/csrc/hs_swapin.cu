@@ -32,12 +32,12 @@
 //      phys[H + j] for miss j, R * (H + C) + q * E + t mod E on the extra
 //      page); hit slots take the call's epoch; first occurrences list their
 //      token, last step and device row;
-//   5. the leader CTA (rank 0) commits the request's policy state on up to
-//      512 of its threads (epoch-CLOCK victims, admission, rotation, index
-//      update), while every other warp of the cluster copies the request's
-//      miss rows from the mapped pinned host pool, claiming 16-byte pieces
-//      from a per-batch-row counter; the commit's warps join the copy when
-//      they are done.
+//   5. the leader CTA (rank 0) commits the request's policy state
+//      (epoch-CLOCK victims, admission, rotation, index update), while the
+//      other CTAs of the cluster copy the request's miss rows from the
+//      mapped pinned host pool, claiming 16-byte pieces from a per-batch-row
+//      counter; the leader joins the copy when it is done.  A cluster of one
+//      CTA commits on 16 of its warps and copies on the others.
 // A request's copy thus starts as soon as its own lookup is complete; no
 // CTA waits for another batch row.  The commit rewrites only policy state,
 // the copy only device KV rows, so the two never touch the same memory.
@@ -224,7 +224,7 @@ __device__ unsigned radix_select(const Group& g, const unsigned* keys, int n, in
 //     (ascending slot): its old token leaves the index, phys[v] and
 //     phys[H + j] swap (the copied row becomes the hot row, no second copy),
 //     the new token enters the index and the slot takes epoch E.
-// `keys` is H words of shared memory.
+// `keys` is H + C words of shared memory: the keys, then the victims.
 __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, int U, int E,
                                unsigned* keys) {
     __shared__ int s_tmp[33];
@@ -242,7 +242,7 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
     long long* bank = a.lv.bank + (long long)q * d.hash_size;
     const unsigned hmask = (unsigned)d.hash_size - 1u;
     const long long wbase = (long long)b * d.C;
-    int32_t* vict = a.ws.vict + wbase;
+    int* vict = reinterpret_cast<int*>(keys + H);  // victims in ascending slot order
     int32_t* adm = a.ws.adm + wbase;
 
     // Keys for victim selection: epoch + 1 (0 = never used), or kHitKey.
@@ -266,34 +266,28 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
         if (bits > 0) thr = radix_select(g, keys, H, m, bits, s_hist, s_sel, &need);
         // Each warp owns a contiguous chunk of slots, read lane by lane, so
         // ballots keep ascending slot order without shared-memory conflicts.
+        // One pass counts each chunk's keys below and at the threshold, one
+        // scan of both counts (packed: each is at most H <= 32768, and fewer
+        // than m keys lie below the threshold) places every chunk, and a
+        // second pass writes the victims: every key below the threshold,
+        // then the lowest `need` slots at it.
         const int lane = tid & 31, warp = tid >> 5, nw = BD >> 5;
         const int chunk = ((H + nw - 1) / nw + 31) & ~31;
         const int w0 = warp * chunk, w1 = min(H, w0 + chunk);
-        int eq = 0;
+        int lt = 0, eq = 0;
         for (int v0 = w0; v0 < w1; v0 += 32) {
             const int v = v0 + lane;
-            eq += __popc(__ballot_sync(0xffffffffu, v < w1 && keys[v] == thr));
+            const unsigned k = v < w1 ? keys[v] : kHitKey;
+            lt += __popc(__ballot_sync(0xffffffffu, k < thr));
+            eq += __popc(__ballot_sync(0xffffffffu, k == thr));
         }
-        int eq_total;
-        const int eq_before = group_exclusive_scan(g, lane == 0 ? eq : 0, s_tmp, &eq_total);
-        const int eq_w = __shfl_sync(0xffffffffu, eq_before, 0);
-        int nv = 0;
+        int packed_total;
+        const int packed_before =
+            group_exclusive_scan(g, lane == 0 ? (lt << 16) | eq : 0, s_tmp, &packed_total);
+        const int pw = __shfl_sync(0xffffffffu, packed_before, 0);
         {
-            int er = eq_w;
-            for (int v0 = w0; v0 < w1; v0 += 32) {
-                const int v = v0 + lane;
-                const unsigned k = v < w1 ? keys[v] : kHitKey;
-                const unsigned em = __ballot_sync(0xffffffffu, k == thr);
-                const bool take = k < thr || (k == thr && er + __popc(em & lanemask_lt()) < need);
-                nv += __popc(__ballot_sync(0xffffffffu, take));
-                er += __popc(em);
-            }
-        }
-        int nv_total;
-        const int v_before = group_exclusive_scan(g, lane == 0 ? nv : 0, s_tmp, &nv_total);
-        {
-            int er = eq_w;
-            int vpos = __shfl_sync(0xffffffffu, v_before, 0);
+            int er = pw & 0xffff;                        // keys at the threshold before the chunk
+            int vpos = (pw >> 16) + (er < need ? er : need);  // victims before the chunk
             for (int v0 = w0; v0 < w1; v0 += 32) {
                 const int v = v0 + lane;
                 const unsigned k = v < w1 ? keys[v] : kHitKey;
@@ -548,13 +542,26 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     {
         int4* f4 = reinterpret_cast<int4*>(first);
         for (int x = tid; x < (TS >> 2); x += BD) f4[x] = make_int4(kNoFirst, kNoFirst, kNoFirst, kNoFirst);
-        int4* m4 = reinterpret_cast<int4*>(smask);
-        for (int x = tid; x < (TS >> 4); x += BD) m4[x] = make_int4(0, 0, 0, 0);
+        if (!BY_POSITION || a.S > 1) {  // step bits (unused by a single-step call)
+            int4* m4 = reinterpret_cast<int4*>(smask);
+            for (int x = tid; x < (TS >> 4); x += BD) m4[x] = make_int4(0, 0, 0, 0);
+        }
         if (!BY_POSITION) {
             int4* k4 = reinterpret_cast<int4*>(keys);
             for (int x = tid; x < (TS >> 2); x += BD) k4[x] = make_int4(-1, -1, -1, -1);
         }
     }
+    // The request lock and epoch, read by the leader's first thread right
+    // away (both in flight together; the epoch only matters if the lock is
+    // won, and nothing else changes it while the lock is held).
+    int lock_old = 0, epoch0 = 0;
+    if (c == 0 && tid == 0 && q_ok) {
+        int32_t* ctrl_q = a.lv.ctrl + (long long)q * kCtrlWords;
+        epoch0 = ctrl_q[CTRL_EPOCH];
+        lock_old = atomicCAS(ctrl_q + CTRL_LOCK, 0, 1);
+    }
+    // The batch row's copy claim counter (16-byte pieces of its miss rows
+    // handed out so far), zeroed by the leader before the first barrier.
     unsigned* claim = reinterpret_cast<unsigned*>(a.ws.cnt + (long long)b * kCntWords + CNT_CLAIM);
     if (c == 0 && tid == 0) *claim = 0u;
     if (tid < 4) s_cnt[tid] = 0;
@@ -589,17 +596,17 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             if (valid) e[r] = bank[pos[r]];
         }
         if (c == 0 && tid == 0) {
-            // The request lock and epoch, decided once and sent to every CTA.
+            // The lock decision and the epoch, sent to every CTA.
             int ok = 1;
             if (!q_ok) {
                 atomicOr(a.ws.status, HS_STATUS_BAD_REQUEST);
                 ok = 0;
-            } else if (atomicCAS(&a.lv.ctrl[(long long)q * kCtrlWords + CTRL_LOCK], 0, 1) != 0) {
+            } else if (lock_old != 0) {
                 atomicOr(a.ws.status, HS_STATUS_DUPLICATE_REQUEST);
                 ok = 0;
             }
             if (sl > d.L) atomicOr(a.ws.status, HS_STATUS_SEQ_LEN_CLAMPED);
-            const int E = ok ? a.lv.ctrl[(long long)q * kCtrlWords + CTRL_EPOCH] : 0;
+            const int E = ok ? epoch0 : 0;
             for (int r = 0; r < P; ++r) {
                 *cluster.map_shared_rank(&s_ok, r) = ok;
                 *cluster.map_shared_rank(&s_epoch, r) = E;
@@ -628,10 +635,6 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             }
         }
     }
-    // Hits: fetch the slot's physical row now (the epoch stamp waits for the lock).
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) aux[r] = code[r] >= 0 ? phys[code[r]] : 0;
-
     // ---- 2. de-duplicate misses into the cluster-wide table ------------------
     if (BY_POSITION) {
 #pragma unroll
@@ -641,8 +644,9 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             const int home = t[r] & (P - 1);
             const int u = t[r] >> plog;
             atomicMin(cluster.map_shared_rank(first, home) + u, i);
-            atomicOr(cluster.map_shared_rank(smask, home) + (u >> 2),
-                     (1u << (i / d.K)) << ((u & 3) * 8));
+            if (a.S > 1)  // a single-step call's last step is always step 0
+                atomicOr(cluster.map_shared_rank(smask, home) + (u >> 2),
+                         (1u << (i / d.K)) << ((u & 3) * 8));
             code[r] = miss_code(u * kMaxCluster + home);
         }
     } else {
@@ -686,12 +690,9 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         return;
     }
     const int E = s_epoch;
-    {
-        int32_t* ep = a.lv.ep + (long long)q * d.H;
+    // Hits: fetch the slot's physical row (used in step 4).
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r)
-            if (code[r] >= 0) ep[code[r]] = E;  // hit slots take the call's epoch
-    }
+    for (int r = 0; r < RMAX; ++r) aux[r] = code[r] >= 0 ? phys[code[r]] : 0;
 
     // ---- 3. first occurrences: flags, running counts, totals -----------------
     {
@@ -703,8 +704,11 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
                 const int x = miss_value(code[r]);
                 const int home = x & (kMaxCluster - 1), u = x >> 3;
                 aux[r] = *(cluster.map_shared_rank(first, home) + u);
-                mw[r] = *(cluster.map_shared_rank(smask, home) + (u >> 2));
-                mw[r] = (mw[r] >> ((u & 3) * 8)) & 0xffu;
+                mw[r] = 1u;
+                if (!BY_POSITION || a.S > 1) {
+                    mw[r] = *(cluster.map_shared_rank(smask, home) + (u >> 2));
+                    mw[r] = (mw[r] >> ((u & 3) * 8)) & 0xffu;
+                }
             }
         }
 #pragma unroll
@@ -753,6 +757,14 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     for (int k = 0; k < P; ++k) U += s_tot[k];
     const long long wbase = (long long)b * d.C;
     {
+        // Hit slots take the call's epoch (the commit reads it after the
+        // cluster barrier below).
+        int32_t* ep = a.lv.ep + (long long)q * d.H;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+            if (code[r] >= 0) ep[code[r]] = E;
+    }
+    {
         int j[RMAX];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {  // remote words of other CTAs' first occurrences
@@ -770,6 +782,12 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
                        __popc((unsigned)wd & ((1u << (l1 & 31)) - 1u));
             }
         }
+        // Every position load in flight before any store below: a store
+        // might alias phys as far as the compiler knows, so loads mixed
+        // with the stores would each wait for the previous round trip.
+        int prow[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) prow[r] = code[r] <= -3 ? phys[d.H + j[r]] : 0;
         int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
@@ -786,7 +804,7 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
                 loc = -1;
                 ++n_inv;
             } else {
-                loc = (int)(base + phys[d.H + j[r]]);
+                loc = (int)(base + prow[r]);
                 ++n_miss;
                 if (miss_value(code[r]) == i) {  // first occurrence: list the miss
                     a.ws.miss_tok[wbase + j[r]] = t[r];
@@ -835,8 +853,10 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         if (a.plan_count) a.plan_count[b] = U;
     }
 
-    // ---- 5. commit on the leader's first warps, copy everywhere else --------
-    const int commit_warps = nwarps < kCommitWarps ? nwarps : kCommitWarps;
+    // ---- 5. commit on the leader, copy everywhere else ----------------------
+    // With other CTAs in the cluster to copy, the whole leader commits (and
+    // copies once it is done); a lone CTA splits its warps between the two.
+    const int commit_warps = P > 1 ? nwarps : (nwarps < kCommitWarps ? nwarps : kCommitWarps);
     if (c == 0 && warp < commit_warps) {
         commit_request(a, Group{tid, commit_warps * 32}, b, q, U, E,
                        reinterpret_cast<unsigned*>(smem));
@@ -881,7 +901,7 @@ cudaError_t launch_one(const SwapArgs& a, const SwapinShape& sh, cudaStream_t s)
 //     rounded up to whole warps, at least 256 (512 with H >= 2048, since
 //     the leader CTA's threads also run the commit over the H slots).
 //   - shared memory: the table share plus the bitmap words, or the commit's
-//     H keys if larger.
+//     H keys and up to C victims if larger.
 SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
     const int N = steps * d.K;
     int p = 1;
@@ -913,7 +933,7 @@ SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
     }
     const size_t table = (size_t)(((sh.by_position ? 5 : 9) * sh.dedup_entries + 15) & ~15);
     const size_t words = (size_t)sh.rmax * (sh.block / 32) * 8;
-    const size_t commit = (size_t)d.H * 4;
+    const size_t commit = (size_t)(d.H + d.C) * 4;  // keys and victims
     sh.smem = table + words > commit ? table + words : commit;
     return sh;
 }

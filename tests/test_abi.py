@@ -30,8 +30,11 @@ def test_header_constants_match_binding():
                  "HS_ERR_DEVICE_STATUS", "HS_ERR_TIMEOUT", "HS_STATUS_BAD_REQUEST",
                  "HS_STATUS_DUPLICATE_REQUEST", "HS_STATUS_SEQ_LEN_CLAMPED",
                  "HS_STATUS_PROBE_LIMIT", "HS_STATUS_TABLE_FULL", "HS_STATUS_BAD_APPEND",
-                 "HS_NUM_STATS", "HS_MAX_EXTRA_PAGE", "HS_STAT_EXTRA", "HS_STATUS_BAD_PLAN"):
+                 "HS_NUM_STATS", "HS_MAX_EXTRA_PAGE", "HS_STAT_EXTRA", "HS_STATUS_BAD_PLAN",
+                 "HS_MAX_ITEM_BYTES"):
         assert int(consts[name], 0) == getattr(B, name), name
+    m = re.search(r"#define HS_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and int(m.group(1)) << int(m.group(2)) == B.HS_NOALLOC_SCRATCH_BYTES
 
 
 def test_version_and_strings(lib):
@@ -70,7 +73,7 @@ def test_sizes(lib):
     st = pkg.hs_state_bytes(c)
     assert st >= R * (16384 * 8 + H * 4 * 2 + (H + C) * 4 + 32)
     assert st % 256 == 0
-    assert pkg.hs_workspace_bytes(c) >= 5 * 64 * C * 4
+    assert pkg.hs_workspace_bytes(c) >= 4 * 64 * C * 4
     assert pkg.hs_state_bytes(_cfg(max_steps=9)) == 0
     assert pkg.hs_hash_size(_cfg(hot_buffer_size=1)) == 32
 
@@ -156,6 +159,10 @@ def test_extra_page_config(lib):
     assert pkg.hs_config_check(_cfg(extra_page_size=-1)) == B.HS_ERR_INVALID_ARG
     assert pkg.hs_config_check(_cfg(extra_page_size=B.HS_MAX_EXTRA_PAGE)) == B.HS_OK
     assert pkg.hs_config_check(_cfg(extra_page_size=B.HS_MAX_EXTRA_PAGE + 1)) == \
+        B.HS_ERR_UNSUPPORTED
+    # rows up to 64 KiB (the copy counts 16-byte pieces of a call in 32 bits)
+    assert pkg.hs_config_check(_cfg(item_size_bytes=B.HS_MAX_ITEM_BYTES)) == B.HS_OK
+    assert pkg.hs_config_check(_cfg(item_size_bytes=B.HS_MAX_ITEM_BYTES + 16)) == \
         B.HS_ERR_UNSUPPORTED
     # device rows must stay addressable by int32 locations
     # (52428 requests of 32768 + 8192 rows are 32767 rows short of 2^31 - 1)
