@@ -481,39 +481,44 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
     return out
 
 
+# Words of the kernel's per-CTA timeline (hs_set_timeline), in phase order.
+TIMELINE_WORDS = (("probed", 1), ("barrier_0", 2), ("inserted", 3), ("table_complete", 4),
+                  ("flagged", 5), ("words_exchanged", 6), ("rows_loaded", 7),
+                  ("lists_written", 8), ("commit_done", 9), ("copy_done", 10))
+TL_START, TL_LISTS, TL_COMMIT, TL_COPY, TL_P = 0, 8, 9, 10, 15
+
+
 def phase_times(tls):
     """Phase spans of each timed launch from the kernel's timeline stamps.
 
-    tls: int64 [launches, batch, 8 ranks, 8 words] as written with
-    hs_set_timeline (words 0-6 global-timer ns, word 7 the cluster size).
+    tls: int64 [launches, batch, 8 ranks, 16 words] as written with
+    hs_set_timeline (words 0-10 global-timer ns, word 15 the cluster size).
     Per launch, with t0 the first CTA's start:
-      gather_span   = last word 4 (locations and miss lists written) - t0;
-      commit_span   = last word 5 of the leader CTAs - their first word 4;
-      commit        = each leader CTA's word 5 - word 4;
-      copy_span     = last word 6 (a CTA's last warp done) - first word 4.
+      gather_span   = last word 8 (locations and miss lists written) - t0;
+      commit_span   = last word 9 of the leader CTAs - their first word 8;
+      commit        = each leader CTA's word 9 - word 8;
+      copy_span     = last word 10 (a CTA's last warp done) - first word 8.
     The summary gives, in microseconds from t0, the median over launches of
     the median and the last CTA at each stamp."""
     tls = np.asarray(tls, dtype=np.int64)
-    names = ("table_cleared", "dedup_done", "counts_exchanged", "lists_written",
-             "commit_done", "copy_done")
     out = {"gather_span_us": [], "commit_span_us": [], "commit_us": [], "copy_span_us": []}
-    marks = {n: ([], []) for n in names}
+    marks = {n: ([], []) for n, _ in TIMELINE_WORDS}
     for t in tls:
-        P = int(t[0, 0, 7])
+        P = int(t[0, 0, TL_P])
         used = t[:, :P, :]
-        t0 = used[:, :, 0].min()
-        out["gather_span_us"].append((used[:, :, 4].max() - t0) / 1e3)
+        t0 = used[:, :, TL_START].min()
+        out["gather_span_us"].append((used[:, :, TL_LISTS].max() - t0) / 1e3)
         lead = t[:, 0, :]
-        out["commit_span_us"].append((lead[:, 5].max() - lead[:, 4].min()) / 1e3)
-        out["commit_us"].extend(((lead[:, 5] - lead[:, 4]) / 1e3).tolist())
-        out["copy_span_us"].append((used[:, :, 6].max() - used[:, :, 4].min()) / 1e3)
-        for k, n in enumerate(names, start=1):
-            v = (lead[:, 5] if n == "commit_done" else used[:, :, k].ravel()) - t0
+        out["commit_span_us"].append((lead[:, TL_COMMIT].max() - lead[:, TL_LISTS].min()) / 1e3)
+        out["commit_us"].extend(((lead[:, TL_COMMIT] - lead[:, TL_LISTS]) / 1e3).tolist())
+        out["copy_span_us"].append((used[:, :, TL_COPY].max() - used[:, :, TL_LISTS].min()) / 1e3)
+        for n, k in TIMELINE_WORDS:
+            v = (lead[:, k] if k == TL_COMMIT else used[:, :, k].ravel()) - t0
             marks[n][0].append(float(np.median(v)) / 1e3)
             marks[n][1].append(float(v.max()) / 1e3)
     out["summary"] = {n: {"median_cta": statistics.median(m[0]), "last_cta": statistics.median(m[1])}
                       for n, m in marks.items()}
-    out["summary"]["cluster_size"] = int(tls[0, 0, 0, 7])
+    out["summary"]["cluster_size"] = int(tls[0, 0, 0, TL_P])
     return out
 
 
@@ -789,8 +794,8 @@ def main():
     # ---- phase split from the kernel's own timeline (separate pass) ----
     # Every CTA stamps the GPU's global timer at its phase boundaries
     # (hs_set_timeline); the launches are direct, each between two events.
-    tl = torch.zeros((Bn, 8, 8), dtype=torch.int64, device=dev)
-    tls = torch.zeros((n_phase, Bn, 8, 8), dtype=torch.int64, device=dev)
+    tl = torch.zeros((Bn, 8, 16), dtype=torch.int64, device=dev)
+    tls = torch.zeros((n_phase, Bn, 8, 16), dtype=torch.int64, device=dev)
     e_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
     e_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_phase)]
     pbase = base + K + PRIMER_STEPS

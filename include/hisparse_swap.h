@@ -344,14 +344,20 @@ int hs_copy_planned(hs_state* st, int32_t layer_id, const int64_t* miss_src_dev,
 
 /* Profiling (no counterpart on the pages): when `timeline_dev` is non-NULL,
  * every later hs_swap_in (and hs_swap_in_noalloc) on this handle writes the
- * phase times of its CTAs there, as uint64 [batch][8][8] indexed by batch
- * row, cluster rank and word (8-byte aligned device memory; rows of ranks
- * the call does not use are left untouched).  Words 0-6 are nanoseconds of
- * the GPU's global timer: 0 CTA start, 1 de-duplication table cleared,
- * 2 lookups and de-duplication done, 3 first-occurrence counts exchanged,
- * 4 locations and miss lists written, 5 commit done (rank 0 only), 6 last
- * warp done copying; word 7 is the cluster size.  A rejected batch row
- * writes words 0-2 and 7 only.  NULL turns it off.  Host only. */
+ * phase times of its CTAs there, as uint64 [batch][8][16] indexed by batch
+ * row, cluster rank and word (8-byte aligned device memory of at least
+ * max_batch * 128 words; rows of ranks the call does not use are left
+ * untouched).  Words 0-10 are nanoseconds of the GPU's global timer, taken
+ * by the CTA's first thread once the data named has arrived: 0 CTA start,
+ * 1 its index probes answered, 2 past the first cluster barrier (the
+ * de-duplication tables cleared), 3 its de-duplication inserts issued,
+ * 4 past the second barrier (the tables complete), 5 its first-occurrence
+ * flags known, 6 past the third barrier (flag words and counts exchanged),
+ * 7 its hit and miss rows loaded, 8 past the fourth barrier (locations and
+ * miss lists written), 9 commit done (rank 0 only), 10 its last warp done
+ * copying.  Word 15 is the cluster size; words 11-14 are unused.  A
+ * rejected batch row writes words 0-4 and 15 only.  Recording costs a few
+ * instructions of each CTA's first thread.  NULL turns it off.  Host only. */
 int hs_set_timeline(hs_state* st, uint64_t* timeline_dev);
 
 /* Tuning: CTAs of hs_copy_planned.  0 restores the default (twice the SM

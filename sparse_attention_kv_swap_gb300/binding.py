@@ -43,6 +43,7 @@ STAT_NAMES = ("hits", "hit_slots", "dup_misses", "unique_misses", "admitted", "e
 HS_MAX_EXTRA_PAGE = 65536
 HS_MAX_ITEM_BYTES = 65536
 HS_NOALLOC_SCRATCH_BYTES = 16 << 20
+TIMELINE_WORDS_PER_ROW = 8 * 16  # hs_set_timeline: [batch][8 ranks][16 words]
 
 HEADER = os.path.join(_build.INCLUDE, "hisparse_swap.h")
 
@@ -446,18 +447,19 @@ def hs_get_stats(handle: StateHandle, layer_id: int, reset: bool = False, stream
 
 
 def hs_set_timeline(handle: StateHandle, timeline=None) -> None:
-    """timeline: a uint64-sized CUDA tensor of at least max_batch * 64
+    """timeline: a uint64-sized CUDA tensor of at least max_batch * 128
     elements on the handle's device (the per-CTA phase stamps of later
-    swap-ins, [batch][8][8]), or None to stop recording."""
+    swap-ins, [batch][8][16]), or None to stop recording."""
     import torch
     ptr = 0
     with _on_device(handle.device):
         if timeline is not None:
             if not timeline.is_cuda:
                 raise ValueError("timeline must be in device memory")
-            if timeline.numel() < handle.cfg.max_batch * 64:
+            if timeline.numel() < handle.cfg.max_batch * TIMELINE_WORDS_PER_ROW:
                 raise ValueError("timeline: need %d elements, got %d"
-                                 % (handle.cfg.max_batch * 64, timeline.numel()))
+                                 % (handle.cfg.max_batch * TIMELINE_WORDS_PER_ROW,
+                                    timeline.numel()))
             ptr = _dptr(timeline, torch.int64, "timeline")
         _check(load_library().hs_set_timeline(handle.ptr, ptr), "hs_set_timeline")
 

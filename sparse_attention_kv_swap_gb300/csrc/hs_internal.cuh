@@ -45,9 +45,24 @@ enum Cnt : int {
     CNT_CLAIM = 0,  // 16-byte pieces of the batch row's miss rows claimed by copying warps
 };
 
-// Words of the optional per-CTA timeline (hs_set_timeline): [b][rank][8].
-constexpr int kTimelineCtas = 8;   // cluster ranks per batch row (P <= 8)
-constexpr int kTimelineWords = 8;  // words per CTA
+// Words of the optional per-CTA timeline (hs_set_timeline): [b][rank][16],
+// global-timer nanoseconds unless noted.
+constexpr int kTimelineCtas = 8;    // cluster ranks per batch row (P <= 8)
+constexpr int kTimelineWords = 16;  // words per CTA
+enum TimelineWord : int {
+    TL_START = 0,         // CTA start
+    TL_PROBED = 1,        // its index probes answered
+    TL_BARRIER0 = 2,      // past the first cluster barrier (tables cleared)
+    TL_INSERTED = 3,      // its de-duplication inserts issued
+    TL_BARRIER_A = 4,     // past the second (tables complete)
+    TL_FLAGGED = 5,       // its first-occurrence flags known
+    TL_BARRIER_B = 6,     // past the third (flag words and counts exchanged)
+    TL_ROWS = 7,          // its hit and miss rows loaded
+    TL_BARRIER_C = 8,     // past the fourth (locations and miss lists written)
+    TL_COMMITTED = 9,     // commit done (leader only)
+    TL_COPIED = 10,       // its last warp done copying
+    TL_CLUSTER_SIZE = 15  // P (a count, not a time)
+};
 
 struct Dims {
     int32_t R, L, W, H, K, S_max, C, layers, B_max;

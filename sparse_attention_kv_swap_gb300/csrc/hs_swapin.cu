@@ -19,8 +19,10 @@
 //      shared memory, which keeps for each token the smallest flat index at
 //      which it occurs and the set of steps it occurs in.  When the table
 //      fits, it is indexed by the token's position (home CTA t mod P, entry
-//      t / P) and an insert is two fire-and-forget atomics; otherwise it is
-//      a hash table with linear probing (compare-and-swap inserts);
+//      t / P) and an insert is one fire-and-forget atomic (two in a
+//      multi-step call); otherwise it is a hash table with linear probing
+//      (compare-and-swap inserts).  Steps 1 and 2 touch no other CTA's
+//      shared memory, so step 1 runs before the first cluster barrier;
 //   3. an entry is the first occurrence of its token iff the table holds its
 //      own flat index.  Each CTA turns its first-occurrence flags into a
 //      bitmap over its entries with a running count per 32-entry word, and
@@ -30,8 +32,8 @@
 //      that CTA's running count and bitmap up to it.  Every entry gets its
 //      device row (q * (H + C) + phys[slot] for a hit, q * (H + C) +
 //      phys[H + j] for miss j, R * (H + C) + q * E + t mod E on the extra
-//      page); hit slots take the call's epoch; first occurrences list their
-//      token, last step and device row;
+//      page); first occurrences list their token, last step and device row.
+//      Hit slots are collected as a bitmap in the leader's shared memory;
 //   5. the leader CTA (rank 0) commits the request's policy state
 //      (epoch-CLOCK victims, admission, rotation, index update), while the
 //      other CTAs of the cluster copy the request's miss rows from the
@@ -57,16 +59,28 @@ constexpr int kCopyUnroll = 6;
 constexpr int kWarpPieces = 32 * kCopyUnroll;  // 16-byte pieces a warp claims at once
 constexpr int kCommitWarps = 16;               // the leader CTA's commit warps (at most)
 constexpr unsigned kHitKey = 0xffffffffu;      // radix key of a slot referenced by the call
+constexpr int kKeyBatch = 8;                    // epochs a commit thread loads at once
 // Shared memory one CTA may spend on its share of a position-indexed
-// de-duplication table (5 bytes a position); longer sequences use the
-// hashed table.
+// de-duplication table (4 bytes a position, 8 for a multi-step call);
+// longer sequences use the hashed table.
 constexpr int kPositionTableBytes = 160 * 1024;
 
 // Entry codes: >= 0 hit slot; -1 invalid; kMissPending; after step 2
 // <= -3 a miss in the de-duplication table at entry (u * 8 + home); after
-// step 3 <= -3 a miss whose token first occurs at flat index (-3 - code).
+// step 3 <= -3 a miss whose token first occurs at flat index
+// (-3 - code) & 0xffff (below HS_MAX_ENTRIES) and last occurs in step
+// (-3 - code) >> 16.
 __device__ __forceinline__ int miss_code(int x) { return -3 - x; }
 __device__ __forceinline__ int miss_value(int code) { return -3 - code; }
+
+// Timeline stamp once the values in v (loads in flight) have arrived: the
+// empty asm consumes each value, so the timer is read after the data.
+template <int N>
+__device__ __forceinline__ void stamp_after(unsigned long long* tl, int word, const int (&v)[N]) {
+#pragma unroll
+    for (int r = 0; r < N; ++r) asm volatile("" ::"r"(v[r]));
+    tl[word] = global_timer();
+}
 
 // Warps [0, n / 32) of the CTA, synchronising on named barrier 1 (the
 // leader CTA's commit warps, while its other warps copy).
@@ -213,8 +227,9 @@ __device__ unsigned radix_select(const Group& g, const unsigned* keys, int n, in
 // Commit of batch row b (request q, epoch E, U unique misses) by group g
 // (section 实现拆解 item 1 of the multi-step swap report; overflow admission
 // prefers the latest step: section 风险与影响):
-//   - hot slots referenced by the call already carry epoch E (step 4 stamped
-//     them), so cap = H - #{ep == E} and m = min(U, cap);
+//   - `hits` has a bit for every hot slot the call referenced: those slots
+//     take epoch E (in the same pass that builds the keys), cap = H - #hits
+//     and m = min(U, cap);
 //   - victims: the m non-hit slots with the smallest (epoch, slot); a radix
 //     select over epoch + 1 finds the threshold epoch and how many slots at
 //     the threshold to take (the lowest ones);
@@ -226,7 +241,7 @@ __device__ unsigned radix_select(const Group& g, const unsigned* keys, int n, in
 //     the new token enters the index and the slot takes epoch E.
 // `keys` is H + C words of shared memory: the keys, then the victims.
 __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, int U, int E,
-                               unsigned* keys) {
+                               const unsigned* hits, unsigned* keys) {
     __shared__ int s_tmp[33];
     __shared__ int s_hist[256];
     __shared__ int s_sel[2];
@@ -245,13 +260,28 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
     int* vict = reinterpret_cast<int*>(keys + H);  // victims in ascending slot order
     int32_t* adm = a.ws.adm + wbase;
 
-    // Keys for victim selection: epoch + 1 (0 = never used), or kHitKey.
+    // Keys for victim selection: epoch + 1 (0 = never used), or kHitKey for
+    // a slot the call referenced, which takes epoch E in the same pass.
+    // Each thread loads kKeyBatch epochs before it stores any, so the loads
+    // are in flight together.
     int nhit = 0;
-    for (int v = tid; v < H; v += BD) {
-        const int e = ep[v];
-        const bool hit = (e == E);
-        keys[v] = hit ? kHitKey : (unsigned)(e + 1);
-        nhit += hit;
+    for (int v0 = tid; v0 < H; v0 += kKeyBatch * BD) {
+        int e[kKeyBatch];
+#pragma unroll
+        for (int u = 0; u < kKeyBatch; ++u) {
+            const int v = v0 + u * BD;
+            e[u] = v < H ? ep[v] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kKeyBatch; ++u) {
+            const int v = v0 + u * BD;
+            if (v < H) {
+                const bool hit = (hits[v >> 5] >> (v & 31)) & 1u;
+                keys[v] = hit ? kHitKey : (unsigned)(e[u] + 1);
+                if (hit) ep[v] = E;
+                nhit += hit;
+            }
+        }
     }
     nhit = group_sum(g, nhit, s_tmp);  // includes the barrier that publishes keys
     const int cap = H - nhit;
@@ -486,8 +516,12 @@ template <int RMAX, bool BY_POSITION>
 __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_ok, s_epoch, s_done;
-    __shared__ int s_tot[kMaxCluster];
-    __shared__ int s_cnt[4];
+    __shared__ int s_tot[kMaxCluster];     // first occurrences of each rank
+    __shared__ int s_cnt[kMaxCluster][4];  // leader: each rank's hit / invalid / miss / extra entries
+    __shared__ int s_wcnt[32][4];          // the same counts per warp of this CTA
+    // Hot slots referenced by this CTA's entries, one bit a slot; the
+    // leader's copy collects every CTA's bits for the commit.
+    __shared__ unsigned s_hits[HS_MAX_HOT_BUFFER / 32];
     cg::cluster_group cluster = cg::this_cluster();
     const int P = (int)cluster.num_blocks();
     const int c = (int)cluster.block_rank();
@@ -503,29 +537,59 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     unsigned long long* tl =
         a.timeline ? a.timeline + ((long long)b * kTimelineCtas + c) * kTimelineWords : nullptr;
     if (tl && tid == 0) {
-        tl[0] = global_timer();
-        tl[7] = (unsigned long long)P;
+        tl[TL_START] = global_timer();
+        tl[TL_CLUSTER_SIZE] = (unsigned long long)P;
     }
 
     // This CTA's share of the de-duplication table, then the bitmap words.
+    // Indexed by position, an entry is the smallest flat index of the token
+    // (int) and, for a multi-step call, the OR of its step bits next to it
+    // (one 8-byte word, read by one load); hashed, the table keeps the
+    // tokens, the smallest flat indices and 8 step bits an entry apart.
     const int TS = a.dedup_entries;
-    int* first = reinterpret_cast<int*>(smem);                  // smallest flat index
-    unsigned* smask = reinterpret_cast<unsigned*>(first + TS);  // 8 step bits an entry
-    int* keys = reinterpret_cast<int*>(smask + (TS >> 2));      // hashed table: the tokens
-    const int table_bytes = ((BY_POSITION ? 5 : 9) * TS + 15) & ~15;
-    // word w = r * nwarps + warp of this CTA's entries: (running count << 32) | flags
+    const bool pairs = BY_POSITION && a.S > 1;
+    int* first = reinterpret_cast<int*>(smem);
+    unsigned* smask = reinterpret_cast<unsigned*>(first + TS);  // hashed table only
+    int* keys = reinterpret_cast<int*>(smask + (TS >> 2));      // hashed table only
+    const int table_bytes = BY_POSITION ? (pairs ? 8 : 4) * TS : (9 * TS + 15) & ~15;
+    // Bitmap words of every rank of the cluster (each CTA sends its own to
+    // all): fw[c' * NW + w], word w = r * nwarps + warp of rank c''s
+    // entries, (running count << 32) | first-occurrence flags.
+    const int NW = RMAX * nwarps;
     unsigned long long* fw = reinterpret_cast<unsigned long long*>(smem + table_bytes);
 
-    // ---- 0. independent loads first: request slot, length, this CTA's entries
+    // ---- 0. loads first (request slot, length, this CTA's entries), then
+    // the table clear, which depends on none of them
     const int q = __ldg(a.rpi + b);
     const int sl = __ldg(a.seq_lens + b);
     const int32_t* topk_b = a.topk + (long long)b * N;
-    int t[RMAX], code[RMAX], aux[RMAX];
+    int t[RMAX], code[RMAX], aux[RMAX], hrow[RMAX];
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) {
         const int i = lo + r * BD + tid;
         t[r] = (i < hi) ? __ldg(topk_b + i) : -1;
     }
+    {
+        int4* f4 = reinterpret_cast<int4*>(first);
+        if (pairs) {
+            for (int x = tid; x < (TS >> 1); x += BD) f4[x] = make_int4(kNoFirst, 0, kNoFirst, 0);
+        } else {
+            for (int x = tid; x < (TS >> 2); x += BD)
+                f4[x] = make_int4(kNoFirst, kNoFirst, kNoFirst, kNoFirst);
+        }
+        if (!BY_POSITION) {
+            int4* m4 = reinterpret_cast<int4*>(smask);
+            for (int x = tid; x < (TS >> 4); x += BD) m4[x] = make_int4(0, 0, 0, 0);
+            int4* k4 = reinterpret_cast<int4*>(keys);
+            for (int x = tid; x < (TS >> 2); x += BD) k4[x] = make_int4(-1, -1, -1, -1);
+        }
+    }
+    // The batch row's copy claim counter (16-byte pieces of its miss rows
+    // handed out so far), zeroed by the leader before the first barrier.
+    unsigned* claim = reinterpret_cast<unsigned*>(a.ws.cnt + (long long)b * kCntWords + CNT_CLAIM);
+    if (c == 0 && tid == 0) *claim = 0u;
+    if (tid == 0) s_done = 0;
+    for (int x = tid; x < ((d.H + 31) >> 5); x += BD) s_hits[x] = 0u;
     const bool q_ok = q >= 0 && q < d.R;
     const int limit = sl < d.L ? sl : d.L;
     // first position of the extra page (past every valid token if none)
@@ -533,49 +597,23 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     unsigned xbits = 0u;  // bit r: entry r is on the extra page
     const long long base = (long long)q * (d.H + d.C);
     const int32_t* phys = a.lv.phys + base;
-    if (q_ok) {
-        // Warm L2 for later steps: the scratch positions (locations of the
-        // misses, step 4) and the epochs (the commit).
-        l2_prefetch(phys + d.H, (size_t)d.C * 4, c * BD + tid, P * BD);
-        if (c == 0) l2_prefetch(a.lv.ep + (long long)q * d.H, (size_t)d.H * 4, tid, BD);
-    }
-    {
-        int4* f4 = reinterpret_cast<int4*>(first);
-        for (int x = tid; x < (TS >> 2); x += BD) f4[x] = make_int4(kNoFirst, kNoFirst, kNoFirst, kNoFirst);
-        if (!BY_POSITION || a.S > 1) {  // step bits (unused by a single-step call)
-            int4* m4 = reinterpret_cast<int4*>(smask);
-            for (int x = tid; x < (TS >> 4); x += BD) m4[x] = make_int4(0, 0, 0, 0);
-        }
-        if (!BY_POSITION) {
-            int4* k4 = reinterpret_cast<int4*>(keys);
-            for (int x = tid; x < (TS >> 2); x += BD) k4[x] = make_int4(-1, -1, -1, -1);
-        }
-    }
-    // The request lock and epoch, read by the leader's first thread right
-    // away (both in flight together; the epoch only matters if the lock is
-    // won, and nothing else changes it while the lock is held).
+    // ---- 1. probe the token -> slot index: global memory only, so it runs
+    // before the first cluster barrier, beside the other CTAs' table clear
     int lock_old = 0, epoch0 = 0;
-    if (c == 0 && tid == 0 && q_ok) {
-        int32_t* ctrl_q = a.lv.ctrl + (long long)q * kCtrlWords;
-        epoch0 = ctrl_q[CTRL_EPOCH];
-        lock_old = atomicCAS(ctrl_q + CTRL_LOCK, 0, 1);
-    }
-    // The batch row's copy claim counter (16-byte pieces of its miss rows
-    // handed out so far), zeroed by the leader before the first barrier.
-    unsigned* claim = reinterpret_cast<unsigned*>(a.ws.cnt + (long long)b * kCntWords + CNT_CLAIM);
-    if (c == 0 && tid == 0) *claim = 0u;
-    if (tid < 4) s_cnt[tid] = 0;
-    if (tid == 0) s_done = 0;
-    cluster.sync();  // every CTA of the cluster runs and its table share is empty
-    if (tl && tid == 0) tl[1] = global_timer();
-
-    // ---- 1. probe the token -> slot index ------------------------------------
     {
         const long long* bank = a.lv.bank + (long long)(q_ok ? q : 0) * d.hash_size;
         const unsigned hmask = (unsigned)d.hash_size - 1u;
         const int16_t* map = a.lv.map + (long long)(q_ok ? q : 0) * d.L;
         long long e[RMAX];
         unsigned pos[RMAX];
+        // The request lock and epoch, read by the leader's first thread
+        // together with its index loads (the epoch only matters if the lock
+        // is won, and nothing else changes it while the lock is held).
+        if (c == 0 && tid == 0 && q_ok) {
+            int32_t* ctrl_q = a.lv.ctrl + (long long)q * kCtrlWords;
+            epoch0 = ctrl_q[CTRL_EPOCH];
+            lock_old = atomicCAS(ctrl_q + CTRL_LOCK, 0, 1);
+        }
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             const bool in_range = q_ok && (lo + r * BD + tid < hi) && t[r] >= 0 && t[r] < limit;
@@ -594,23 +632,6 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             }
             pos[r] = hash_token(t[r], d.hash_shift);
             if (valid) e[r] = bank[pos[r]];
-        }
-        if (c == 0 && tid == 0) {
-            // The lock decision and the epoch, sent to every CTA.
-            int ok = 1;
-            if (!q_ok) {
-                atomicOr(a.ws.status, HS_STATUS_BAD_REQUEST);
-                ok = 0;
-            } else if (lock_old != 0) {
-                atomicOr(a.ws.status, HS_STATUS_DUPLICATE_REQUEST);
-                ok = 0;
-            }
-            if (sl > d.L) atomicOr(a.ws.status, HS_STATUS_SEQ_LEN_CLAMPED);
-            const int E = ok ? epoch0 : 0;
-            for (int r = 0; r < P; ++r) {
-                *cluster.map_shared_rank(&s_ok, r) = ok;
-                *cluster.map_shared_rank(&s_epoch, r) = E;
-            }
         }
         if (!d.dense) {
 #pragma unroll
@@ -635,6 +656,43 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             }
         }
     }
+    if (tl && tid == 0) stamp_after(tl, TL_PROBED, code);
+    cluster.sync();  // every CTA of the cluster runs and its table share is empty
+    if (tl && tid == 0) tl[TL_BARRIER0] = global_timer();
+
+    // Hits: mark the slot for the commit and load its physical row (used in
+    // step 4; these loads complete while the next barrier waits anyway).
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+        hrow[r] = 0;
+        if (code[r] >= 0) {
+            atomicOr(&s_hits[code[r] >> 5], 1u << (code[r] & 31));
+            hrow[r] = phys[code[r]];
+        }
+    }
+    if (q_ok) {
+        // Warm L2 for later steps: the scratch positions (miss locations,
+        // step 4) and the epochs (the commit).
+        l2_prefetch(phys + d.H, (size_t)d.C * 4, c * BD + tid, P * BD);
+        if (c == 0) l2_prefetch(a.lv.ep + (long long)q * d.H, (size_t)d.H * 4, tid, BD);
+    }
+    if (c == 0 && tid == 0) {
+        // The lock decision and the epoch, sent to every CTA.
+        int ok = 1;
+        if (!q_ok) {
+            atomicOr(a.ws.status, HS_STATUS_BAD_REQUEST);
+            ok = 0;
+        } else if (lock_old != 0) {
+            atomicOr(a.ws.status, HS_STATUS_DUPLICATE_REQUEST);
+            ok = 0;
+        }
+        if (sl > d.L) atomicOr(a.ws.status, HS_STATUS_SEQ_LEN_CLAMPED);
+        const int E = ok ? epoch0 : 0;
+        for (int r = 0; r < P; ++r) {
+            *cluster.map_shared_rank(&s_ok, r) = ok;
+            *cluster.map_shared_rank(&s_epoch, r) = E;
+        }
+    }
     // ---- 2. de-duplicate misses into the cluster-wide table ------------------
     if (BY_POSITION) {
 #pragma unroll
@@ -643,10 +701,10 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             const int i = lo + r * BD + tid;
             const int home = t[r] & (P - 1);
             const int u = t[r] >> plog;
-            atomicMin(cluster.map_shared_rank(first, home) + u, i);
-            if (a.S > 1)  // a single-step call's last step is always step 0
-                atomicOr(cluster.map_shared_rank(smask, home) + (u >> 2),
-                         (1u << (i / d.K)) << ((u & 3) * 8));
+            int* f = cluster.map_shared_rank(first, home) + (pairs ? 2 * u : u);
+            atomicMin(f, i);
+            if (pairs)  // a single-step call's last step is always step 0
+                atomicOr(reinterpret_cast<unsigned*>(f + 1), 1u << (i / d.K));
             code[r] = miss_code(u * kMaxCluster + home);
         }
     } else {
@@ -676,8 +734,9 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             }
         }
     }
+    if (tl && tid == 0) tl[TL_INSERTED] = global_timer();
     cluster.sync();  // the table is complete, s_ok / s_epoch have arrived
-    if (tl && tid == 0) tl[2] = global_timer();
+    if (tl && tid == 0) tl[TL_BARRIER_A] = global_timer();
 
     int32_t* locs_b = a.locs + (long long)b * N;
     if (!s_ok) {
@@ -690,9 +749,6 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         return;
     }
     const int E = s_epoch;
-    // Hits: fetch the slot's physical row (used in step 4).
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) aux[r] = code[r] >= 0 ? phys[code[r]] : 0;
 
     // ---- 3. first occurrences: flags, running counts, totals -----------------
     {
@@ -703,37 +759,66 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             if (code[r] <= -3) {
                 const int x = miss_value(code[r]);
                 const int home = x & (kMaxCluster - 1), u = x >> 3;
-                aux[r] = *(cluster.map_shared_rank(first, home) + u);
-                mw[r] = 1u;
-                if (!BY_POSITION || a.S > 1) {
+                if (!BY_POSITION) {
+                    aux[r] = *(cluster.map_shared_rank(first, home) + u);
                     mw[r] = *(cluster.map_shared_rank(smask, home) + (u >> 2));
                     mw[r] = (mw[r] >> ((u & 3) * 8)) & 0xffu;
+                } else if (pairs) {  // first index and step bits in one load
+                    const unsigned long long v = *reinterpret_cast<const unsigned long long*>(
+                        cluster.map_shared_rank(first, home) + 2 * u);
+                    aux[r] = (int)(unsigned)v;
+                    mw[r] = (unsigned)(v >> 32);
+                } else {
+                    aux[r] = *(cluster.map_shared_rank(first, home) + u);
+                    mw[r] = 1u;
                 }
             }
         }
+        int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             const int i = lo + r * BD + tid;
             const bool f = code[r] <= -3 && aux[r] == i;
-            if (code[r] <= -3) {
-                code[r] = miss_code(aux[r]);     // now: first index of the token
-                aux[r] = 31 - __clz((int)mw[r]);  // last step in which it occurs
+            if (i < hi) {  // the counters of this CTA's entries
+                if ((xbits >> r) & 1u) ++n_ext;
+                else if (code[r] >= 0) ++n_hit;
+                else if (code[r] == -1) ++n_inv;
+                else ++n_miss;
             }
+            if (code[r] <= -3)  // now: the token's first index and last step
+                code[r] = miss_code(aux[r] | ((31 - __clz((int)mw[r])) << 16));
             const unsigned bal = __ballot_sync(0xffffffffu, f);
-            if (lane == 0) fw[r * nwarps + warp] = bal;
+            if (lane == 0) fw[c * NW + r * nwarps + warp] = bal;
+        }
+        n_hit = __reduce_add_sync(0xffffffffu, n_hit);
+        n_inv = __reduce_add_sync(0xffffffffu, n_inv);
+        n_miss = __reduce_add_sync(0xffffffffu, n_miss);
+        n_ext = __reduce_add_sync(0xffffffffu, n_ext);
+        if (lane == 0) {
+            s_wcnt[warp][0] = n_hit;
+            s_wcnt[warp][1] = n_inv;
+            s_wcnt[warp][2] = n_miss;
+            s_wcnt[warp][3] = n_ext;
         }
     }
+    if (tl && tid == 0) stamp_after(tl, TL_FLAGGED, code);
     __syncthreads();
+    if (c != 0) {  // this CTA's hit slots, into the leader's bitmap
+        unsigned* lead = cluster.map_shared_rank(s_hits, 0);
+        for (int x = tid; x < ((d.H + 31) >> 5); x += BD)
+            if (s_hits[x]) atomicOr(lead + x, s_hits[x]);
+    }
     if (warp == 0) {
-        // running counts over the RMAX * nwarps words in (r, warp) order
-        const int n = RMAX * nwarps;
-        const int per_lane = (n + 31) >> 5;
+        // Running counts over this CTA's RMAX * nwarps words in (r, warp)
+        // order; each finished word goes to every CTA of the cluster, so
+        // that step 4 reads any rank's words from its own shared memory.
+        const int per_lane = (NW + 31) >> 5;
         unsigned bw[RMAX];
         int sum = 0;
 #pragma unroll
         for (int k = 0; k < RMAX; ++k) {
             const int idx = lane * per_lane + k;
-            bw[k] = (k < per_lane && idx < n) ? (unsigned)fw[idx] : 0u;
+            bw[k] = (k < per_lane && idx < NW) ? (unsigned)fw[c * NW + idx] : 0u;
             sum += __popc(bw[k]);
         }
         const int inc = warp_inclusive_scan(sum);
@@ -741,54 +826,54 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
 #pragma unroll
         for (int k = 0; k < RMAX; ++k) {
             const int idx = lane * per_lane + k;
-            if (k < per_lane && idx < n) {
-                fw[idx] = ((unsigned long long)(unsigned)run << 32) | bw[k];
+            if (k < per_lane && idx < NW) {
+                fw[c * NW + idx] = ((unsigned long long)(unsigned)run << 32) | bw[k];
                 run += __popc(bw[k]);
             }
         }
+        __syncwarp();
+        for (int rk = 1; rk < P; ++rk) {
+            unsigned long long* dst = cluster.map_shared_rank(fw + c * NW, (c + rk) & (P - 1));
+            for (int idx = lane; idx < NW; idx += 32) dst[idx] = fw[c * NW + idx];
+        }
         const int total = __shfl_sync(0xffffffffu, inc, 31);
         if (lane < P) *cluster.map_shared_rank(&s_tot[c], lane) = total;
+        if (lane < 4) {  // this CTA's entry counters, to the leader
+            int n = 0;
+            for (int w = 0; w < nwarps; ++w) n += s_wcnt[w][lane];
+            *cluster.map_shared_rank(&s_cnt[c][lane], 0) = n;
+        }
     }
-    cluster.sync();  // every CTA's words and total are in place
-    if (tl && tid == 0) tl[3] = global_timer();
+    cluster.sync();  // every CTA's words, totals and counters are in place
+    if (tl && tid == 0) tl[TL_BARRIER_B] = global_timer();
 
-    // ---- 4. ordinals, locations, miss lists, counters -----------------------
+    // ---- 4. ordinals, locations, miss lists ---------------------------------
     int U = 0;
     for (int k = 0; k < P; ++k) U += s_tot[k];
     const long long wbase = (long long)b * d.C;
     {
-        // Hit slots take the call's epoch (the commit reads it after the
-        // cluster barrier below).
-        int32_t* ep = a.lv.ep + (long long)q * d.H;
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r)
-            if (code[r] >= 0) ep[code[r]] = E;
-    }
-    {
         int j[RMAX];
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r) {  // remote words of other CTAs' first occurrences
+        for (int r = 0; r < RMAX; ++r) {  // ordinal of the token's first occurrence
             j[r] = 0;
             if (code[r] <= -3) {
-                const int i1 = miss_value(code[r]);
+                const int i1 = miss_value(code[r]) & 0xffff;
                 const int c1 = i1 / per;
                 const int l1 = i1 - c1 * per;
-                const unsigned long long wd = c1 == c
-                                                  ? fw[l1 >> 5]
-                                                  : *(cluster.map_shared_rank(fw, c1) + (l1 >> 5));
+                const unsigned long long wd = fw[c1 * NW + (l1 >> 5)];
                 int off = 0;
                 for (int k = 0; k < c1; ++k) off += s_tot[k];
-                j[r] = off + (int)(wd >> 32) +
-                       __popc((unsigned)wd & ((1u << (l1 & 31)) - 1u));
+                j[r] = off + (int)(wd >> 32) + __popc((unsigned)wd & ((1u << (l1 & 31)) - 1u));
             }
         }
         // Every position load in flight before any store below: a store
         // might alias phys as far as the compiler knows, so loads mixed
         // with the stores would each wait for the previous round trip.
-        int prow[RMAX];
+        int row[RMAX];
 #pragma unroll
-        for (int r = 0; r < RMAX; ++r) prow[r] = code[r] <= -3 ? phys[d.H + j[r]] : 0;
-        int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
+        for (int r = 0; r < RMAX; ++r)
+            row[r] = code[r] >= 0 ? hrow[r] : (code[r] <= -3 ? phys[d.H + j[r]] : 0);
+        if (tl && tid == 0) stamp_after(tl, TL_ROWS, row);
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             const int i = lo + r * BD + tid;
@@ -796,19 +881,15 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             int loc;
             if ((xbits >> r) & 1u) {
                 loc = (int)((long long)d.R * (d.H + d.C) + (long long)q * d.E + t[r] % d.E);
-                ++n_ext;
             } else if (code[r] >= 0) {
-                loc = (int)(base + aux[r]);
-                ++n_hit;
+                loc = (int)(base + row[r]);
             } else if (code[r] == -1) {
                 loc = -1;
-                ++n_inv;
             } else {
-                loc = (int)(base + prow[r]);
-                ++n_miss;
-                if (miss_value(code[r]) == i) {  // first occurrence: list the miss
+                loc = (int)(base + row[r]);
+                if ((miss_value(code[r]) & 0xffff) == i) {  // first occurrence: list the miss
                     a.ws.miss_tok[wbase + j[r]] = t[r];
-                    a.ws.miss_last[wbase + j[r]] = aux[r];
+                    a.ws.miss_last[wbase + j[r]] = miss_value(code[r]) >> 16;
                     a.ws.miss_dst[wbase + j[r]] = loc;
                     if (a.plan_src) {
                         a.plan_src[wbase + j[r]] = (long long)q * d.L + t[r];
@@ -818,38 +899,33 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             }
             locs_b[i] = loc;
         }
-        n_hit = __reduce_add_sync(0xffffffffu, n_hit);
-        n_inv = __reduce_add_sync(0xffffffffu, n_inv);
-        n_miss = __reduce_add_sync(0xffffffffu, n_miss);
-        n_ext = __reduce_add_sync(0xffffffffu, n_ext);
-        if (lane == 0) {
-            int* rc = cluster.map_shared_rank(s_cnt, 0);
-            atomicAdd(&rc[0], n_hit);
-            atomicAdd(&rc[1], n_inv);
-            atomicAdd(&rc[2], n_miss);
-            if (n_ext) atomicAdd(&rc[3], n_ext);
-        }
     }
-    // Counters complete, miss lists and epoch stamps visible to the whole
-    // cluster; no shared memory of another CTA is touched after this point.
+    // Miss lists visible to the whole cluster; no shared memory of another
+    // CTA is touched after this point.
     cluster.sync();
-    if (tl && tid == 0) tl[4] = global_timer();
+    if (tl && tid == 0) tl[TL_BARRIER_C] = global_timer();
     if (c == 0 && tid == 0) {
-        const int n_hit = s_cnt[0], n_inv = s_cnt[1], n_miss = s_cnt[2];
+        int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
+        for (int k = 0; k < P; ++k) {
+            n_hit += s_cnt[k][0];
+            n_inv += s_cnt[k][1];
+            n_miss += s_cnt[k][2];
+            n_ext += s_cnt[k][3];
+        }
         if (a.stats) {
             int32_t* st = a.stats + (long long)b * HS_NUM_STATS;
             st[HS_STAT_HITS] = n_hit;
             st[HS_STAT_DUP_MISSES] = n_miss - U;
             st[HS_STAT_UNIQUE_MISSES] = U;
             st[HS_STAT_INVALID] = n_inv;
-            st[HS_STAT_EXTRA] = s_cnt[3];
+            st[HS_STAT_EXTRA] = n_ext;
         }
         unsigned long long* tot = a.lv.totals;  // the layer's running sums
         atomicAdd(tot + HS_STAT_HITS, (unsigned long long)n_hit);
         atomicAdd(tot + HS_STAT_DUP_MISSES, (unsigned long long)(n_miss - U));
         atomicAdd(tot + HS_STAT_UNIQUE_MISSES, (unsigned long long)U);
         atomicAdd(tot + HS_STAT_INVALID, (unsigned long long)n_inv);
-        atomicAdd(tot + HS_STAT_EXTRA, (unsigned long long)s_cnt[3]);
+        atomicAdd(tot + HS_STAT_EXTRA, (unsigned long long)n_ext);
         if (a.plan_count) a.plan_count[b] = U;
     }
 
@@ -858,14 +934,14 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     // copies once it is done); a lone CTA splits its warps between the two.
     const int commit_warps = P > 1 ? nwarps : (nwarps < kCommitWarps ? nwarps : kCommitWarps);
     if (c == 0 && warp < commit_warps) {
-        commit_request(a, Group{tid, commit_warps * 32}, b, q, U, E,
+        commit_request(a, Group{tid, commit_warps * 32}, b, q, U, E, s_hits,
                        reinterpret_cast<unsigned*>(smem));
-        if (tl && tid == 0) tl[5] = global_timer();
+        if (tl && tid == 0) tl[TL_COMMITTED] = global_timer();
     }
     if (!a.defer_copy && U > 0)
         copy_request(a.lv.host_pool + (long long)q * d.L * d.W, a.lv.device_kv,
                      a.ws.miss_tok + wbase, a.ws.miss_dst + wbase, U, d.W, claim);
-    if (tl && lane == 0 && atomicAdd(&s_done, 1) == nwarps - 1) tl[6] = global_timer();
+    if (tl && lane == 0 && atomicAdd(&s_done, 1) == nwarps - 1) tl[TL_COPIED] = global_timer();
 }
 
 template <int RMAX, bool BY_POSITION>
@@ -899,19 +975,23 @@ cudaError_t launch_one(const SwapArgs& a, const SwapinShape& sh, cudaStream_t s)
 //     kPositionTableBytes per CTA.  If it never fits, the table is hashed.
 //   - threads: 1024 for more than 1024 entries per CTA, else the entries
 //     rounded up to whole warps, at least 256 (512 with H >= 2048, since
-//     the leader CTA's threads also run the commit over the H slots).
-//   - shared memory: the table share plus the bitmap words, or the commit's
-//     H keys and up to C victims if larger.
+//     the leader CTA's threads also run the commit over the H slots).  More
+//     threads than entries would not pay: with one 1024-thread CTA per SM,
+//     clusters of 8 no longer all fit at once (16 of them in a 152-SM
+//     GB300 ran in two waves).
+//   - shared memory: the table share plus the bitmap words of every rank,
+//     or the commit's H keys and up to C victims if larger.
 SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
     const int N = steps * d.K;
     int p = 1;
     while (p < kMaxCluster && batch * (2 * p) <= sms && N / (2 * p) >= 256) p *= 2;
     while (p < kMaxCluster && (N + p - 1) / p > 4096) p *= 2;
     auto pos_entries = [&](int pp) { return ((d.L + pp - 1) / pp + 15) & ~15; };
+    const int entry_bytes = steps > 1 ? 8 : 4;  // first index (+ step bits)
     int pp = p;
-    while (pp < kMaxCluster && 5 * pos_entries(pp) > kPositionTableBytes) pp *= 2;
+    while (pp < kMaxCluster && entry_bytes * pos_entries(pp) > kPositionTableBytes) pp *= 2;
     SwapinShape sh;
-    sh.by_position = 5 * pos_entries(pp) <= kPositionTableBytes;
+    sh.by_position = entry_bytes * pos_entries(pp) <= kPositionTableBytes;
     if (sh.by_position) p = pp;
     sh.P = p;
     if (sh.by_position) {
@@ -931,8 +1011,9 @@ SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
         sh.rmax = per <= 2048 ? 2 : 4;
         sh.block = 1024;
     }
-    const size_t table = (size_t)(((sh.by_position ? 5 : 9) * sh.dedup_entries + 15) & ~15);
-    const size_t words = (size_t)sh.rmax * (sh.block / 32) * 8;
+    const size_t table = sh.by_position ? (size_t)entry_bytes * sh.dedup_entries
+                                        : (size_t)((9 * sh.dedup_entries + 15) & ~15);
+    const size_t words = (size_t)p * sh.rmax * (sh.block / 32) * 8;  // every rank's words
     const size_t commit = (size_t)(d.H + d.C) * 4;  // keys and victims
     sh.smem = table + words > commit ? table + words : commit;
     return sh;

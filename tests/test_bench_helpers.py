@@ -87,26 +87,27 @@ def test_phase_times_reads_the_kernel_timeline():
     """Two launches of a 3-row call in clusters of 2 (ns stamps): spans from
     the first CTA's start, the leaders' commits and the copy window."""
     import numpy as np
-    t = np.zeros((2, 3, 8, 8), np.int64)
+    t = np.zeros((2, 3, 8, 16), np.int64)
     for launch in range(2):
         for b in range(3):
             for r in range(2):
-                t[launch, b, r, :7] = [1000 + 10 * b, 2000, 3000, 4000, 5000 + 100 * b,
-                                       0, 9000 + 10 * r]
-                t[launch, b, r, 7] = 2
-            t[launch, b, 0, 5] = 7000 + 500 * b
+                t[launch, b, r, :11] = [1000 + 10 * b, 1500, 2000, 2500, 3000, 3500, 4000,
+                                        4500, 5000 + 100 * b, 0, 9000 + 10 * r]
+                t[launch, b, r, 15] = 2
+            t[launch, b, 0, 9] = 7000 + 500 * b
     out = bench.phase_times(t)
-    # gather: last word 4 (5200) minus the first start (1000)
+    # gather: last word 8 (5200) minus the first start (1000)
     assert out["gather_span_us"] == [4.2, 4.2]
-    # commit span: last leader word 5 (8000) minus the first leader word 4 (5000)
+    # commit span: last leader word 9 (8000) minus the first leader word 8 (5000)
     assert out["commit_span_us"] == [3.0, 3.0]
     assert sorted(out["commit_us"]) == [2.0, 2.0, 2.4, 2.4, 2.8, 2.8]
-    # copy window: last word 6 (9010) minus the first word 4 (5000)
+    # copy window: last word 10 (9010) minus the first word 8 (5000)
     assert out["copy_span_us"] == [4.01, 4.01]
     s = out["summary"]
     assert s["cluster_size"] == 2
+    assert s["probed"]["median_cta"] == 0.5  # word 1 (1500) from t0 = 1000
     assert s["lists_written"]["last_cta"] == 4.2
     assert s["commit_done"]["last_cta"] == 7.0
-    # a rank the call does not use (word 7 tells the cluster size) is ignored
+    # a rank the call does not use (word 15 tells the cluster size) is ignored
     t[:, :, 2:, :] = 123456789
     assert bench.phase_times(t)["gather_span_us"] == [4.2, 4.2]

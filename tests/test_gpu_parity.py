@@ -294,31 +294,33 @@ def test_hashed_dedup_for_sequences_beyond_the_position_table(dense):
 
 
 def test_timeline_stamps_are_ordered_and_change_nothing():
-    """hs_set_timeline: every used CTA writes its phase stamps in order, the
-    leader its commit stamp, word 7 the cluster size; results stay exact."""
+    """hs_set_timeline: every used CTA writes its phase stamps (words 0-8
+    and 10) in order, the leader its commit stamp (word 9), word 15 the
+    cluster size, nothing else; results stay exact."""
     import torch
     import sparse_attention_kv_swap_gb300 as pkg
     w = W.scaled(W.WORKLOADS["C3"], batch=4, seq_len=16384)
     stream = W.TopkStream(w)
     rpi, sl = W.req_pool_indices(w), W.seq_lens(w)
     run = ParityRun(w.batch, w.seq_len, w.row_bytes, w.hot_buffer, w.top_k, w.steps, dense=True)
-    tl = torch.zeros(w.batch * 64, dtype=torch.int64, device="cuda")
+    tl = torch.zeros(w.batch * 128, dtype=torch.int64, device="cuda")
     pkg.hs_set_timeline(run.cache.handle, tl)
     for c in range(3):
         tl.zero_()
         run.call(stream.next_call(), rpi, sl)
-        t = tl.view(w.batch, 8, 8).cpu().numpy()
-        P = int(t[0, 0, 7])
-        assert P in (1, 2, 4, 8) and (t[:, :P, 7] == P).all() and (t[:, P:] == 0).all()
+        t = tl.view(w.batch, 8, 16).cpu().numpy()
+        P = int(t[0, 0, 15])
+        assert P in (1, 2, 4, 8) and (t[:, :P, 15] == P).all() and (t[:, P:] == 0).all()
+        assert (t[:, :P, 11:15] == 0).all()
         for b in range(w.batch):
             for r in range(P):
                 s = t[b, r]
-                assert (s[:5] > 0).all() and (np.diff(s[:5]) >= 0).all(), (b, r, s)
-                assert s[6] >= s[4], (b, r, s)
+                assert (s[:9] > 0).all() and (np.diff(s[:9]) >= 0).all(), (b, r, s)
+                assert s[10] >= s[8], (b, r, s)
                 if r == 0:
-                    assert s[4] <= s[5] <= s[6], (b, s)
+                    assert s[8] <= s[9] <= s[10], (b, s)
                 else:
-                    assert s[5] == 0, (b, r, s)
+                    assert s[9] == 0, (b, r, s)
     pkg.hs_set_timeline(run.cache.handle, None)
     tl.zero_()
     run.call(stream.next_call(), rpi, sl)
