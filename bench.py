@@ -952,8 +952,7 @@ def main():
 
     traffic = NCU_TRAFFIC.get((args.config, args.index), {})
     gather_hbm = dict(hbm_phase(gather_bytes, timeline["gather_span_us"]),
-                      span="first CTA start to the last CTA's locations and miss lists",
-                      traffic=traffic.get("gather_dram_bytes"))
+                      span="first CTA start to the last CTA's locations and miss lists")
     commit_hbm = dict(hbm_phase(commit_bytes, timeline["commit_span_us"]),
                       span="first leader CTA's commit start to the last one's end "
                            "(each request's commit starts when its own lookup ends)",
@@ -1001,6 +1000,14 @@ def main():
             "timeline_us": timeline["summary"],
             "gather_hbm": gather_hbm,
             "commit_hbm": commit_hbm,
+            "dram_traffic": {
+                "bytes_per_launch": traffic.get("dram_bytes"),
+                "lookup_commit_algorithmic_bytes": float(np.mean(gather_bytes + commit_bytes)),
+                "ratio": (traffic["dram_bytes"] / float(np.mean(gather_bytes + commit_bytes))
+                          if traffic else None),
+                "note": "DRAM read + write bytes of the whole launch (ncu, " + NCU_CAPTURE
+                        + ") over the lookup's and the commit's algorithmic bytes; the copy's "
+                          "device writes mostly stay in L2 within the launch"},
             "copy_window": {"gbs": float(np.mean(copy_window)), "peak": h2d_peak,
                             "frac": float(np.mean(copy_window)) / h2d_peak,
                             "span": "first lookup end to the last warp's copy end"},

@@ -168,7 +168,7 @@ struct SwapinShape {
     int dedup_entries; // entries of one CTA's share of that table
     size_t smem;    // dynamic shared memory per CTA
 };
-SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms);
+SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms, int p_cap);
 
 // Launchers (each returns the launch's error code).
 cudaError_t launch_swapin(const SwapArgs& a, int sms, cudaStream_t s);

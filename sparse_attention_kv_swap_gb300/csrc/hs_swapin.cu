@@ -945,34 +945,104 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
 }
 
 template <int RMAX, bool BY_POSITION>
-cudaError_t launch_one(const SwapArgs& a, const SwapinShape& sh, cudaStream_t s) {
+SmemOptIn* smem_opt_in() {
     static SmemOptIn opt_in;
-    cudaError_t e = ensure_smem(swapin_kernel<RMAX, BY_POSITION>, sh.smem, &opt_in);
-    if (e != cudaSuccess) return e;
+    return &opt_in;
+}
+
+// The launch configuration of a shape (attrs: one cluster-dimension attribute).
+inline cudaLaunchConfig_t launch_config(const SwapinShape& sh, int batch, cudaStream_t s,
+                                        cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.B * sh.P);
+    cfg.gridDim = dim3(batch * sh.P);
     cfg.blockDim = dim3(sh.block);
     cfg.dynamicSmemBytes = sh.smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = sh.P;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int RMAX, bool BY_POSITION>
+cudaError_t launch_one(const SwapArgs& a, const SwapinShape& sh, cudaStream_t s) {
+    cudaError_t e = ensure_smem(swapin_kernel<RMAX, BY_POSITION>, sh.smem,
+                                smem_opt_in<RMAX, BY_POSITION>());
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(sh, a.B, s, attr);
     return cudaLaunchKernelEx(&cfg, swapin_kernel<RMAX, BY_POSITION>, a);
+}
+
+// How many clusters of this shape the current device runs at once (0 if
+// the query fails).
+template <int RMAX, bool BY_POSITION>
+int max_clusters_one(const SwapinShape& sh) {
+    if (ensure_smem(swapin_kernel<RMAX, BY_POSITION>, sh.smem, smem_opt_in<RMAX, BY_POSITION>()) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(sh, 1, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, swapin_kernel<RMAX, BY_POSITION>, &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// max_clusters_one, remembered per device and shape (a host query per
+// distinct shape, not per call).
+int max_clusters(const SwapinShape& sh) {
+    struct Entry {
+        int device, rmax, by_position, P, block;
+        size_t smem;
+        int clusters;
+    };
+    static std::mutex m;
+    static Entry cache[128];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    {
+        std::lock_guard<std::mutex> lock(m);
+        for (int i = 0; i < used; ++i) {
+            const Entry& e = cache[i];
+            if (e.device == dev && e.rmax == sh.rmax && e.by_position == (int)sh.by_position &&
+                e.P == sh.P && e.block == sh.block && e.smem == sh.smem)
+                return e.clusters;
+        }
+    }
+    int n = 0;
+    if (sh.by_position)
+        n = sh.rmax == 1 ? max_clusters_one<1, true>(sh)
+                         : (sh.rmax == 2 ? max_clusters_one<2, true>(sh) : max_clusters_one<4, true>(sh));
+    else
+        n = sh.rmax == 1 ? max_clusters_one<1, false>(sh)
+                         : (sh.rmax == 2 ? max_clusters_one<2, false>(sh) : max_clusters_one<4, false>(sh));
+    std::lock_guard<std::mutex> lock(m);
+    if (n > 0 && used < 128)
+        cache[used++] = Entry{dev, sh.rmax, (int)sh.by_position, sh.P, sh.block, sh.smem, n};
+    return n;
 }
 
 }  // namespace
 
 // Launch shape of a call with `batch` rows of `steps * K` entries:
-//   - P, the CTAs per batch row: the largest power of two <= 8 with
+//   - P, the CTAs per batch row: the largest power of two <= p_cap with
 //     batch * P CTAs still within one wave of `sms` SMs and at least 256
 //     entries per CTA, but never more than 4096 entries per CTA (4 a
-//     thread); then raised (up to 8) until a position-indexed
+//     thread); then raised (up to p_cap) until a position-indexed
 //     de-duplication table over max_seq_len positions fits
 //     kPositionTableBytes per CTA.  If it never fits, the table is hashed.
+//     The launcher lowers p_cap while the device cannot hold the batch's
+//     clusters at once.
 //   - threads: 1024 for more than 1024 entries per CTA, else the entries
 //     rounded up to whole warps, at least 256 (512 with H >= 2048, since
 //     the leader CTA's threads also run the commit over the H slots).  More
@@ -981,15 +1051,15 @@ cudaError_t launch_one(const SwapArgs& a, const SwapinShape& sh, cudaStream_t s)
 //     GB300 ran in two waves).
 //   - shared memory: the table share plus the bitmap words of every rank,
 //     or the commit's H keys and up to C victims if larger.
-SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
+SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms, int p_cap) {
     const int N = steps * d.K;
     int p = 1;
-    while (p < kMaxCluster && batch * (2 * p) <= sms && N / (2 * p) >= 256) p *= 2;
+    while (p < p_cap && batch * (2 * p) <= sms && N / (2 * p) >= 256) p *= 2;
     while (p < kMaxCluster && (N + p - 1) / p > 4096) p *= 2;
     auto pos_entries = [&](int pp) { return ((d.L + pp - 1) / pp + 15) & ~15; };
     const int entry_bytes = steps > 1 ? 8 : 4;  // first index (+ step bits)
     int pp = p;
-    while (pp < kMaxCluster && entry_bytes * pos_entries(pp) > kPositionTableBytes) pp *= 2;
+    while (pp < p_cap && entry_bytes * pos_entries(pp) > kPositionTableBytes) pp *= 2;
     SwapinShape sh;
     sh.by_position = entry_bytes * pos_entries(pp) <= kPositionTableBytes;
     if (sh.by_position) p = pp;
@@ -1020,7 +1090,19 @@ SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms) {
 }
 
 cudaError_t launch_swapin(const SwapArgs& a, int sms, cudaStream_t s) {
-    const SwapinShape sh = swapin_shape(a.d, a.B, a.S, sms);
+    SwapinShape sh = swapin_shape(a.d, a.B, a.S, sms, kMaxCluster);
+    // A shape counts CTAs against SMs, but whether clusters of P large CTAs
+    // are co-resident depends on how the SMs group: while the batch would
+    // need more than one wave of clusters, try half the cluster size.
+    while (sh.P > 1) {
+        const int fit = max_clusters(sh);
+        if (fit <= 0 || a.B <= fit) break;
+        const SwapinShape smaller = swapin_shape(a.d, a.B, a.S, sms, sh.P / 2);
+        if (smaller.P >= sh.P) break;
+        const int fit2 = max_clusters(smaller);
+        if (fit2 <= 0 || (a.B + fit2 - 1) / fit2 >= (a.B + fit - 1) / fit) break;  // no fewer waves
+        sh = smaller;
+    }
     SwapArgs g = a;
     g.dedup_entries = sh.dedup_entries;
     g.dedup_shift = 32 - __builtin_ctz((unsigned)(sh.dedup_entries * sh.P));

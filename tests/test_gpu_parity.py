@@ -325,3 +325,52 @@ def test_timeline_stamps_are_ordered_and_change_nothing():
     tl.zero_()
     run.call(stream.next_call(), rpi, sl)
     assert int(tl.abs().sum()) == 0
+
+
+# (batch, steps, top_k, max_seq_len, expected cluster size P, entries a thread, table)
+LAUNCH_SHAPES = [
+    (1, 1, 300, 5000, 1, 1, "position"),
+    (100, 1, 2048, 5000, 1, 2, "position"),
+    (100, 2, 2048, 5000, 1, 4, "position"),
+    (40, 1, 2048, 5000, 2, 1, "position"),
+    (40, 2, 2048, 5000, 2, 2, "position"),
+    (40, 4, 2048, 5000, 2, 4, "position"),
+    (20, 1, 2048, 5000, 4, 1, "position"),
+    (20, 4, 2048, 5000, 4, 2, "position"),
+    (2, 4, 2048, 5000, 8, 1, "position"),
+    (4, 1, 600, 300000, 8, 1, "position"),    # cluster raised until the table fits
+    (40, 4, 2048, 300000, 2, 4, "hashed"),    # too long for a position table
+    # 16 clusters of 8 one-per-SM CTAs do not fit the GPCs at once: the
+    # launcher halves the cluster to keep the call in one wave
+    (16, 4, 2048, 5000, 4, 2, "position"),
+]
+
+
+@pytest.mark.parametrize("Bn,S,K,L,P,rmax,table", LAUNCH_SHAPES)
+def test_every_launch_shape(Bn, S, K, L, P, rmax, table):
+    """Each cluster size and entries-a-thread combination the launch can pick
+    (on a 152-SM GB300), with both kinds of de-duplication table and the
+    fallback to a smaller cluster when the batch's clusters would not be
+    co-resident: the timeline's cluster-size word shows the shape, and two
+    calls match the oracle bit for bit."""
+    import torch
+    import sparse_attention_kv_swap_gb300 as pkg
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("launch shapes are stated for 152 SMs")
+    rng = np.random.default_rng(Bn * 31 + S * 7 + L)
+    run = ParityRun(Bn, L, 16, 512, K, S, dense=(table == "position"))
+    tl = torch.zeros(Bn * 128, dtype=torch.int64, device="cuda")
+    pkg.hs_set_timeline(run.cache.handle, tl)
+    rpi = rng.permutation(Bn).astype(np.int32)
+    sl = np.full(Bn, L, dtype=np.int32)
+    prev = None
+    for c in range(2):
+        topk = rng.integers(0, L, size=(Bn, S, K)).astype(np.int32)
+        if prev is not None:
+            topk[:, 0, :K // 2] = prev[:, -1, K // 2:]
+        for s in range(1, S):
+            topk[:, s, :K // 3] = topk[:, s - 1, -(K // 3):]
+        prev = topk
+        run.call(topk, rpi, sl, compare_rows=(c == 1))
+        t = tl.view(Bn, 8, 16).cpu().numpy()
+        assert int(t[0, 0, 15]) == P, "cluster size %d, expected %d" % (t[0, 0, 15], P)
