@@ -431,7 +431,7 @@ def deferred_copy_pipeline(torch, pkg, w, dev, flush, calls, pool, dense, layers
     s0 = torch.cuda.current_stream()
     # two copy streams, alternating by layer, so that one layer's copy can
     # start while the previous one drains; 32 CTAs per copy keep the link full
-    # and leave the SMs that the next layer's gather needs
+    # and leave the SMs that the next layer's lookup needs
     copy_streams = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
     done = [torch.cuda.Event() for _ in range(layers)]
 

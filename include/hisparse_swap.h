@@ -125,7 +125,7 @@ typedef struct hs_config {
                                 see below                                          */
 } hs_config;
 
-/* Extra page (the gather's first lookup, ahead of the hot-cache hash: "[HiSparse]
+/* Extra page (the first lookup of the report's gather, ahead of the hot-cache hash: "[HiSparse]
  * Support hisparse multi-step swap io kernel", 实现拆解 item 1; the page does not
  * define it, and this library reads it as the request's newest, still-filling
  * page).  With E > 0 every request q owns E device rows, and for a call with

@@ -3,7 +3,7 @@
 // Decode keeps idle KV in host memory (PR #20343 summary, 功能与动机), so
 // every row that decode produces is written to the request's host pool row;
 // the same row also goes to the request's extra page (its newest,
-// still-filling page, which the gather serves without a lookup: "[HiSparse]
+// still-filling page, which the swap-in serves without a lookup: "[HiSparse]
 // Support hisparse multi-step swap io kernel", 实现拆解 item 1) when the
 // position lies on it, and to the token's hot row when the token is
 // resident, so that every copy of (q, t) stays equal.

@@ -35,7 +35,7 @@ enum Ctrl : int {
     CTRL_EPOCH = 0,     // epoch of the next call
     CTRL_RESIDENT = 1,  // tokens resident in the hot slots
     CTRL_USED = 2,      // hash entries not empty (live + deleted)
-    CTRL_LOCK = 3,      // held from gather to commit of one call
+    CTRL_LOCK = 3,      // held from the lookup to the commit of one call
     CTRL_REBUILDS = 4,  // hash rebuilds so far (diagnostic)
 };
 

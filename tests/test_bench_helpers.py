@@ -96,7 +96,7 @@ def test_phase_times_reads_the_kernel_timeline():
                 t[launch, b, r, 15] = 2
             t[launch, b, 0, 9] = 7000 + 500 * b
     out = bench.phase_times(t)
-    # gather: last word 8 (5200) minus the first start (1000)
+    # lookup: last word 8 (5200) minus the first start (1000)
     assert out["gather_span_us"] == [4.2, 4.2]
     # commit span: last leader word 9 (8000) minus the first leader word 8 (5000)
     assert out["commit_span_us"] == [3.0, 3.0]

@@ -1,6 +1,6 @@
 """Extra page and write-back on the GPU against the CPU oracle, bit for bit.
 
-The extra page is the request's newest, still-filling page: the gather
+The extra page is the request's newest, still-filling page: the swap-in
 serves a selected token on it from the page's device row before any
 hot-cache lookup (the multi-step swap report, 实现拆解 item 1).  Decode
 writes each new row back to the host pool (PR #20343 summary, 功能与动机)

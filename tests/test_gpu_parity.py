@@ -1,6 +1,6 @@
 """CUDA path against the CPU oracle, bit for bit (needs a GB300).
 
-Small cases span several gather tiles (1024 entries per tile row), ragged
+Small cases span several CTAs of a request (up to 1024 entries a pass), ragged
 top-k widths, every step count, overflow and multiple layers; the workload
 cases run the five configurations' index streams, scaled where marked and at
 full size where the oracle still finishes in seconds.
