@@ -579,14 +579,15 @@ def multi_vs_sequential(torch, pkg, w, dev, flush, calls, pool, dense, n=20, war
         load(c)
         torch.cuda.synchronize()
         timed = i >= PREROLL_CALLS + warmup
-        for g, acc in ((g_multi, t_m), (g_seq, t_s)):
+        pair = ((g_multi, t_m), (g_seq, t_s))
+        for g, acc in (pair if i % 2 == 0 else pair[::-1]):  # alternate which runs first
             flush.fill_(i & 0xFF)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             with torch.cuda.stream(stream):  # replay runs on the current stream
-                # a 0.1 ms device-side hold so that the graph launch is queued
+                # a 1 ms device-side hold so that the graph launch is queued
                 # before event `a` runs (too short for the clocks to drop)
-                torch.cuda._sleep(int(2e5))
+                torch.cuda._sleep(int(2e6))
                 a.record(stream)
                 g.replay()
                 b.record(stream)

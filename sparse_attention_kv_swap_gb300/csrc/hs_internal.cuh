@@ -109,6 +109,7 @@ struct SwapArgs {
     int32_t defer_copy;   // 1: record the plan only, copy no rows
     unsigned long long* timeline;  // [B][kTimelineCtas][kTimelineWords] or null
     // set by the launcher:
+    int32_t step_bits;      // 1: record each miss's last step (the call may overflow)
     int32_t dedup_entries;  // entries of one CTA's share of the miss de-duplication table
     int32_t dedup_shift;    // hash de-duplication: 32 - log2(P * dedup_entries)
 };
@@ -169,6 +170,7 @@ struct SwapinShape {
     size_t smem;    // dynamic shared memory per CTA
 };
 SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms, int p_cap);
+bool step_bits_needed(const Dims& d, int steps);
 
 // Launchers (each returns the launch's error code).
 cudaError_t launch_swapin(const SwapArgs& a, int sms, cudaStream_t s);

@@ -20,7 +20,8 @@
 //      which it occurs and the set of steps it occurs in.  When the table
 //      fits, it is indexed by the token's position (home CTA t mod P, entry
 //      t / P) and an insert is one fire-and-forget atomic (two in a
-//      multi-step call); otherwise it is a hash table with linear probing
+//      multi-step call that may overflow); otherwise it is a hash table
+//      with linear probing
 //      (compare-and-swap inserts).  Steps 1 and 2 touch no other CTA's
 //      shared memory, so step 1 runs before the first cluster barrier;
 //   3. an entry is the first occurrence of its token iff the table holds its
@@ -61,7 +62,7 @@ constexpr int kCommitWarps = 16;               // the leader CTA's commit warps 
 constexpr unsigned kHitKey = 0xffffffffu;      // radix key of a slot referenced by the call
 constexpr int kKeyBatch = 8;                    // epochs a commit thread loads at once
 // Shared memory one CTA may spend on its share of a position-indexed
-// de-duplication table (4 bytes a position, 8 for a multi-step call);
+// de-duplication table (4 bytes a position, 8 when the call may overflow);
 // longer sequences use the hashed table.
 constexpr int kPositionTableBytes = 160 * 1024;
 
@@ -429,8 +430,11 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
             }
             fresh += bank_insert(bank, d.hash_shift, hmask, t, v, a.ws.status);
         }
-        evicted = group_sum(g, evicted, s_tmp);
-        fresh = group_sum(g, fresh, s_tmp);
+        {  // one scan of both counts (each at most m <= C <= HS_MAX_ENTRIES = 8192)
+            const int both = group_sum(g, (fresh << 16) | evicted, s_tmp);
+            evicted = both & 0xffff;
+            fresh = both >> 16;
+        }
         if (tid == 0) {
             s_misc[0] = ctrl[CTRL_USED] + fresh;
             s_misc[1] = ctrl[CTRL_RESIDENT] + m - evicted;
@@ -543,11 +547,14 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
 
     // This CTA's share of the de-duplication table, then the bitmap words.
     // Indexed by position, an entry is the smallest flat index of the token
-    // (int) and, for a multi-step call, the OR of its step bits next to it
-    // (one 8-byte word, read by one load); hashed, the table keeps the
+    // (int) and, when the call may overflow, the OR of its step bits next to
+    // it (one 8-byte word, read by one load); hashed, the table keeps the
     // tokens, the smallest flat indices and 8 step bits an entry apart.
+    // Only overflow admission reads a miss's last step, and a call with
+    // S * K <= H cannot overflow: its distinct tokens, hits and misses
+    // together, are at most S * K, so U <= H - #hit slots.
     const int TS = a.dedup_entries;
-    const bool pairs = BY_POSITION && a.S > 1;
+    const bool pairs = BY_POSITION && a.step_bits;
     int* first = reinterpret_cast<int*>(smem);
     unsigned* smask = reinterpret_cast<unsigned*>(first + TS);  // hashed table only
     int* keys = reinterpret_cast<int*>(smask + (TS >> 2));      // hashed table only
@@ -703,7 +710,7 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             const int u = t[r] >> plog;
             int* f = cluster.map_shared_rank(first, home) + (pairs ? 2 * u : u);
             atomicMin(f, i);
-            if (pairs)  // a single-step call's last step is always step 0
+            if (pairs)  // else the last step is never read (recorded as step 0)
                 atomicOr(reinterpret_cast<unsigned*>(f + 1), 1u << (i / d.K));
             code[r] = miss_code(u * kMaxCluster + home);
         }
@@ -1034,6 +1041,12 @@ int max_clusters(const SwapinShape& sh) {
 
 }  // namespace
 
+// Whether a call must record each miss's last step: only overflow
+// admission reads it, and a call of S * K <= H entries cannot overflow.
+bool step_bits_needed(const Dims& d, int steps) {
+    return steps > 1 && (long long)steps * d.K > d.H;
+}
+
 // Launch shape of a call with `batch` rows of `steps * K` entries:
 //   - P, the CTAs per batch row: the largest power of two <= p_cap with
 //     batch * P CTAs still within one wave of `sms` SMs and at least 256
@@ -1057,7 +1070,7 @@ SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms, int p_cap
     while (p < p_cap && batch * (2 * p) <= sms && N / (2 * p) >= 256) p *= 2;
     while (p < kMaxCluster && (N + p - 1) / p > 4096) p *= 2;
     auto pos_entries = [&](int pp) { return ((d.L + pp - 1) / pp + 15) & ~15; };
-    const int entry_bytes = steps > 1 ? 8 : 4;  // first index (+ step bits)
+    const int entry_bytes = step_bits_needed(d, steps) ? 8 : 4;  // first index (+ step bits)
     int pp = p;
     while (pp < p_cap && entry_bytes * pos_entries(pp) > kPositionTableBytes) pp *= 2;
     SwapinShape sh;
@@ -1104,6 +1117,7 @@ cudaError_t launch_swapin(const SwapArgs& a, int sms, cudaStream_t s) {
         sh = smaller;
     }
     SwapArgs g = a;
+    g.step_bits = step_bits_needed(a.d, a.S) ? 1 : 0;
     g.dedup_entries = sh.dedup_entries;
     g.dedup_shift = 32 - __builtin_ctz((unsigned)(sh.dedup_entries * sh.P));
     if (sh.by_position) {
