@@ -21,20 +21,21 @@
 //      fits, it is indexed by the token's position (home CTA t mod P, entry
 //      t / P) and an insert is one fire-and-forget atomic (two in a
 //      multi-step call that may overflow); otherwise it is a hash table
-//      with linear probing
-//      (compare-and-swap inserts).  Steps 1 and 2 touch no other CTA's
-//      shared memory, so step 1 runs before the first cluster barrier;
+//      with linear probing (compare-and-swap inserts).  Step 1 touches no
+//      other CTA's shared memory, so it runs before the first cluster
+//      barrier; hit slots are marked in a shared-memory bitmap;
 //   3. an entry is the first occurrence of its token iff the table holds its
-//      own flat index.  Each CTA turns its first-occurrence flags into a
-//      bitmap over its entries with a running count per 32-entry word, and
-//      sends its total to every CTA of the cluster;
+//      own flat index.  Each CTA turns its first-occurrence flags into
+//      64-bit words (running count << 32 | flags of 32 entries) and sends
+//      them, its total, its entry counters and its hit bits to the other
+//      CTAs of the cluster (the hit bits to the leader only);
 //   4. the ordinal j of a miss is the number of first occurrences before
 //      its token's first occurrence: the totals of lower-ranked CTAs plus
-//      that CTA's running count and bitmap up to it.  Every entry gets its
-//      device row (q * (H + C) + phys[slot] for a hit, q * (H + C) +
-//      phys[H + j] for miss j, R * (H + C) + q * E + t mod E on the extra
-//      page); first occurrences list their token, last step and device row.
-//      Hit slots are collected as a bitmap in the leader's shared memory;
+//      that CTA's running count and flags up to it, all read from local
+//      shared memory.  Every entry gets its device row (q * (H + C) +
+//      phys[slot] for a hit, q * (H + C) + phys[H + j] for miss j,
+//      R * (H + C) + q * E + t mod E on the extra page); first occurrences
+//      list their token, last step and device row;
 //   5. the leader CTA (rank 0) commits the request's policy state
 //      (epoch-CLOCK victims, admission, rotation, index update), while the
 //      other CTAs of the cluster copy the request's miss rows from the
