@@ -131,13 +131,16 @@ Workspace workspace_view(const Dims& d, uint8_t* ws);
 // The dynamic shared-memory size a kernel has been opened up to, per device
 // (cudaFuncSetAttribute acts on the calling thread's current device).  Reads
 // are lock-free; raising the limit takes the mutex, so that concurrent host
-// threads leave the attribute and the remembered size equal.
+// threads leave the attribute and the remembered size equal.  Nothing is
+// assumed open at first: without the attribute, static plus dynamic shared
+// memory must stay within 48 KB, so the limit a kernel starts with depends
+// on its own static arrays.
 struct SmemOptIn {
     static constexpr int kMaxDevices = 64;
     std::atomic<int> bytes[kMaxDevices];
     std::mutex raise;
     SmemOptIn() {
-        for (auto& b : bytes) b.store(48 * 1024, std::memory_order_relaxed);
+        for (auto& b : bytes) b.store(0, std::memory_order_relaxed);
     }
 };
 
@@ -145,7 +148,7 @@ struct SmemOptIn {
 // least `bytes`; repeated calls cost one atomic load.
 template <typename F>
 cudaError_t ensure_smem(F* kernel, size_t bytes, SmemOptIn* opt) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes == 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
