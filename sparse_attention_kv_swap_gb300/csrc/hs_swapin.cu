@@ -67,13 +67,28 @@ constexpr int kKeyBatch = 8;                    // epochs a commit thread loads 
 // longer sequences use the hashed table.
 constexpr int kPositionTableBytes = 160 * 1024;
 
+// Entry keys: the entry at local index l (flat index lo + l) of cluster
+// rank c has key c * kKeyStride + l.  Keys order entries as their flat
+// indices do (l < per <= HS_MAX_ENTRIES = kKeyStride), fit in 16 bits for
+// up to 8 ranks, and give the owning rank and local index by shift and
+// mask, where the flat index would need a division by per.
+constexpr int kKeyShift = 13;
+constexpr int kKeyStride = 1 << kKeyShift;
+static_assert(kKeyStride >= HS_MAX_ENTRIES && kMaxCluster * kKeyStride <= 0x10000,
+              "entry keys must cover a rank's entries and fit in 16 bits");
+
 // Entry codes: >= 0 hit slot; -1 invalid; kMissPending; after step 2
 // <= -3 a miss in the de-duplication table at entry (u * 8 + home); after
-// step 3 <= -3 a miss whose token first occurs at flat index
-// (-3 - code) & 0xffff (below HS_MAX_ENTRIES) and last occurs in step
-// (-3 - code) >> 16.
+// step 3 <= -3 a miss whose token first occurs at the entry with key
+// (-3 - code) & 0xffff and last occurs in step (-3 - code) >> 16.
 __device__ __forceinline__ int miss_code(int x) { return -3 - x; }
 __device__ __forceinline__ int miss_value(int code) { return -3 - code; }
+
+// Step of flat index i < S * K (S <= HS_MAX_STEPS = 4), without a division.
+__device__ __forceinline__ int step_of(int i, int K) {
+    return (i >= K) + (i >= 2 * K) + (i >= 3 * K);
+}
+static_assert(HS_MAX_STEPS <= 4, "step_of covers four steps");
 
 // Timeline stamp once the values in v (loads in flight) have arrived: the
 // empty asm consumes each value, so the timer is read after the data.
@@ -117,19 +132,19 @@ __device__ int group_sum(const Group& g, int x, int* tmp) {
     return total;
 }
 
-// Hashed de-duplication: inserts token t (flat index i, step bits `steps`)
+// Hashed de-duplication: inserts token t (entry key `key`, step bits `steps`)
 // into its home CTA's share (already mapped into this CTA's view) starting
 // at `start`; returns the entry.  The whole table has at least twice as
 // many entries as the request has entries, so a free one always exists.
 __device__ __forceinline__ int dedup_insert(int* keys, int* first, unsigned* smask, int size,
-                                            unsigned start, int t, int i, unsigned steps,
+                                            unsigned start, int t, int key, unsigned steps,
                                             uint32_t* status) {
     const unsigned mask = (unsigned)size - 1u;
     unsigned p = start;
     for (int n = 0; n < size; ++n) {
         const int k = atomicCAS(&keys[p], -1, t);
         if (k == -1 || k == t) {
-            atomicMin(&first[p], i);
+            atomicMin(&first[p], key);
             atomicOr(&smask[p >> 2], steps << ((p & 3u) * 8u));
             return (int)p;
         }
@@ -706,26 +721,26 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             if (code[r] != kMissPending) continue;
-            const int i = lo + r * BD + tid;
             const int home = t[r] & (P - 1);
             const int u = t[r] >> plog;
             int* f = cluster.map_shared_rank(first, home) + (pairs ? 2 * u : u);
-            atomicMin(f, i);
+            atomicMin(f, c * kKeyStride + r * BD + tid);
             if (pairs)  // else the last step is never read (recorded as step 0)
-                atomicOr(reinterpret_cast<unsigned*>(f + 1), 1u << (i / d.K));
+                atomicOr(reinterpret_cast<unsigned*>(f + 1),
+                         1u << step_of(lo + r * BD + tid, d.K));
             code[r] = miss_code(u * kMaxCluster + home);
         }
     } else {
         const int ts_log = __ffs(TS) - 1;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
-            const int i = lo + r * BD + tid;
             const bool miss = code[r] == kMissPending;
             // equal tokens of one warp insert once, by their lowest lane
             const unsigned grp = __match_any_sync(0xffffffffu, miss ? t[r] : (-2 - lane));
             if (miss) {
                 const int leader = __ffs(grp) - 1;
-                const unsigned steps = __reduce_or_sync(grp, 1u << (i / d.K));
+                const unsigned steps =
+                    __reduce_or_sync(grp, 1u << step_of(lo + r * BD + tid, d.K));
                 int x = -1;
                 if (lane == leader) {
                     const unsigned h = hash_token(t[r], a.dedup_shift);
@@ -733,7 +748,8 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
                     const int u = dedup_insert(cluster.map_shared_rank(keys, home),
                                                cluster.map_shared_rank(first, home),
                                                cluster.map_shared_rank(smask, home), TS,
-                                               h & (unsigned)(TS - 1), t[r], i, steps,
+                                               h & (unsigned)(TS - 1), t[r],
+                                               c * kKeyStride + r * BD + tid, steps,
                                                a.ws.status);
                     x = u >= 0 ? u * kMaxCluster + home : -1;
                 }
@@ -786,7 +802,7 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             const int i = lo + r * BD + tid;
-            const bool f = code[r] <= -3 && aux[r] == i;
+            const bool f = code[r] <= -3 && aux[r] == c * kKeyStride + r * BD + tid;
             if (i < hi) {  // the counters of this CTA's entries
                 if ((xbits >> r) & 1u) ++n_ext;
                 else if (code[r] >= 0) ++n_hit;
@@ -856,23 +872,31 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     if (tl && tid == 0) tl[TL_BARRIER_B] = global_timer();
 
     // ---- 4. ordinals, locations, miss lists ---------------------------------
-    int U = 0;
-    for (int k = 0; k < P; ++k) U += s_tot[k];
+    // Lane k < P: the first occurrences of the ranks below k (ranks P .. 7
+    // add none); U, all of them.
+    const int tot_k = lane < P ? s_tot[lane] : 0;
+    int incl = tot_k;
+#pragma unroll
+    for (int o = 1; o < kMaxCluster; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int U = __shfl_sync(0xffffffffu, incl, kMaxCluster - 1);
+    const int excl = incl - tot_k;
     const long long wbase = (long long)b * d.C;
     {
         int j[RMAX];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {  // ordinal of the token's first occurrence
-            j[r] = 0;
-            if (code[r] <= -3) {
-                const int i1 = miss_value(code[r]) & 0xffff;
-                const int c1 = i1 / per;
-                const int l1 = i1 - c1 * per;
-                const unsigned long long wd = fw[c1 * NW + (l1 >> 5)];
-                int off = 0;
-                for (int k = 0; k < c1; ++k) off += s_tot[k];
-                j[r] = off + (int)(wd >> 32) + __popc((unsigned)wd & ((1u << (l1 & 31)) - 1u));
-            }
+            // Rank c1 and local index l1 of the first occurrence, from its
+            // key; computed for every entry (the shuffle needs all lanes)
+            // and used for misses only.
+            const bool m = code[r] <= -3;
+            const int key = miss_value(code[r]) & 0xffff;
+            const int c1 = key >> kKeyShift, l1 = key & (kKeyStride - 1);
+            const int off = __shfl_sync(0xffffffffu, excl, c1 & (kMaxCluster - 1));
+            const unsigned long long wd = m ? fw[c1 * NW + (l1 >> 5)] : 0ull;
+            j[r] = m ? off + (int)(wd >> 32) + __popc((unsigned)wd & ((1u << (l1 & 31)) - 1u)) : 0;
         }
         // Every position load in flight before any store below: a store
         // might alias phys as far as the compiler knows, so loads mixed
@@ -895,7 +919,8 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
                 loc = -1;
             } else {
                 loc = (int)(base + row[r]);
-                if ((miss_value(code[r]) & 0xffff) == i) {  // first occurrence: list the miss
+                if ((miss_value(code[r]) & 0xffff) == c * kKeyStride + r * BD + tid) {
+                    // first occurrence: list the miss
                     a.ws.miss_tok[wbase + j[r]] = t[r];
                     a.ws.miss_last[wbase + j[r]] = miss_value(code[r]) >> 16;
                     a.ws.miss_dst[wbase + j[r]] = loc;
