@@ -84,6 +84,17 @@ static_assert(kKeyStride >= HS_MAX_ENTRIES && kMaxCluster * kKeyStride <= 0x1000
 __device__ __forceinline__ int miss_code(int x) { return -3 - x; }
 __device__ __forceinline__ int miss_value(int code) { return -3 - code; }
 
+// The two halves of a cluster barrier (barrier.cluster.arrive / wait, with
+// release and acquire semantics): a thread arrives once its writes for the
+// other CTAs are issued and waits only where it needs theirs, so work that
+// needs neither runs in between.  Called by whole warps.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Step of flat index i < S * K (S <= HS_MAX_STEPS = 4), without a division.
 __device__ __forceinline__ int step_of(int i, int K) {
     return (i >= K) + (i >= 2 * K) + (i >= 3 * K);
@@ -608,11 +619,15 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         }
     }
     // The batch row's copy claim counter (16-byte pieces of its miss rows
-    // handed out so far), zeroed by the leader before the first barrier.
+    // handed out so far), zeroed by the leader after the first barrier (a
+    // global store before that barrier's release would hold it back).
     unsigned* claim = reinterpret_cast<unsigned*>(a.ws.cnt + (long long)b * kCntWords + CNT_CLAIM);
-    if (c == 0 && tid == 0) *claim = 0u;
     if (tid == 0) s_done = 0;
     for (int x = tid; x < ((d.H + 31) >> 5); x += BD) s_hits[x] = 0u;
+    // First barrier, first half: this CTA runs and its table share is
+    // empty.  The second half waits after the probe, which needs no other
+    // CTA, so the barrier costs the probe nothing.
+    cluster_arrive();
     const bool q_ok = q >= 0 && q < d.R;
     const int limit = sl < d.L ? sl : d.L;
     // first position of the extra page (past every valid token if none)
@@ -621,7 +636,7 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     const long long base = (long long)q * (d.H + d.C);
     const int32_t* phys = a.lv.phys + base;
     // ---- 1. probe the token -> slot index: global memory only, so it runs
-    // before the first cluster barrier, beside the other CTAs' table clear
+    // inside the first cluster barrier, beside the other CTAs' table clear
     int lock_old = 0, epoch0 = 0;
     {
         const long long* bank = a.lv.bank + (long long)(q_ok ? q : 0) * d.hash_size;
@@ -680,25 +695,10 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         }
     }
     if (tl && tid == 0) stamp_after(tl, TL_PROBED, code);
-    cluster.sync();  // every CTA of the cluster runs and its table share is empty
+    cluster_wait();  // every CTA of the cluster runs and its table share is empty
     if (tl && tid == 0) tl[TL_BARRIER0] = global_timer();
+    if (c == 0 && tid == 0) *claim = 0u;  // read by the copy, after the last barrier
 
-    // Hits: mark the slot for the commit and load its physical row (used in
-    // step 4; these loads complete while the next barrier waits anyway).
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-        hrow[r] = 0;
-        if (code[r] >= 0) {
-            atomicOr(&s_hits[code[r] >> 5], 1u << (code[r] & 31));
-            hrow[r] = phys[code[r]];
-        }
-    }
-    if (q_ok) {
-        // Warm L2 for later steps: the scratch positions (miss locations,
-        // step 4) and the epochs (the commit).
-        l2_prefetch(phys + d.H, (size_t)d.C * 4, c * BD + tid, P * BD);
-        if (c == 0) l2_prefetch(a.lv.ep + (long long)q * d.H, (size_t)d.H * 4, tid, BD);
-    }
     if (c == 0 && tid == 0) {
         // The lock decision and the epoch, sent to every CTA.
         int ok = 1;
@@ -759,7 +759,26 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         }
     }
     if (tl && tid == 0) tl[TL_INSERTED] = global_timer();
-    cluster.sync();  // the table is complete, s_ok / s_epoch have arrived
+    // Second barrier, first half: this CTA's inserts (and, from the leader,
+    // the lock decision) are sent.  Inside it, the work on hits, which needs
+    // no other CTA: mark the slot for the commit and load its physical row
+    // (used by the next step's locations).
+    cluster_arrive();
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+        hrow[r] = 0;
+        if (code[r] >= 0) {
+            atomicOr(&s_hits[code[r] >> 5], 1u << (code[r] & 31));
+            hrow[r] = phys[code[r]];
+        }
+    }
+    if (q_ok) {
+        // Warm L2 for later steps: the scratch positions (miss locations,
+        // step 4) and the epochs (the commit).
+        l2_prefetch(phys + d.H, (size_t)d.C * 4, c * BD + tid, P * BD);
+        if (c == 0) l2_prefetch(a.lv.ep + (long long)q * d.H, (size_t)d.H * 4, tid, BD);
+    }
+    cluster_wait();  // the table is complete, s_ok / s_epoch have arrived
     if (tl && tid == 0) tl[TL_BARRIER_A] = global_timer();
 
     int32_t* locs_b = a.locs + (long long)b * N;
@@ -827,10 +846,21 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
     }
     if (tl && tid == 0) stamp_after(tl, TL_FLAGGED, code);
     __syncthreads();
-    if (c != 0) {  // this CTA's hit slots, into the leader's bitmap
+    // Warp 0 sends the flag words and the total, warp 1 the entry counters,
+    // the other warps the hit bits (a CTA has at least 8 warps).
+    if (c != 0 && warp >= 2) {  // this CTA's hit slots, into the leader's bitmap
         unsigned* lead = cluster.map_shared_rank(s_hits, 0);
-        for (int x = tid; x < ((d.H + 31) >> 5); x += BD)
+        for (int x = tid - 64; x < ((d.H + 31) >> 5); x += BD - 64)
             if (s_hits[x]) atomicOr(lead + x, s_hits[x]);
+    }
+    if (warp == 1) {  // this CTA's entry counters, to the leader
+        int n[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            n[k] = __reduce_add_sync(0xffffffffu, lane < nwarps ? s_wcnt[lane][k] : 0);
+        if (lane < 4)
+            *cluster.map_shared_rank(&s_cnt[c][lane], 0) =
+                lane == 0 ? n[0] : lane == 1 ? n[1] : lane == 2 ? n[2] : n[3];
     }
     if (warp == 0) {
         // Running counts over this CTA's RMAX * nwarps words in (r, warp)
@@ -862,16 +892,11 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         }
         const int total = __shfl_sync(0xffffffffu, inc, 31);
         if (lane < P) *cluster.map_shared_rank(&s_tot[c], lane) = total;
-        if (lane < 4) {  // this CTA's entry counters, to the leader
-            int n = 0;
-            for (int w = 0; w < nwarps; ++w) n += s_wcnt[w][lane];
-            *cluster.map_shared_rank(&s_cnt[c][lane], 0) = n;
-        }
     }
     cluster.sync();  // every CTA's words, totals and counters are in place
     if (tl && tid == 0) tl[TL_BARRIER_B] = global_timer();
 
-    // ---- 4. ordinals, locations, miss lists ---------------------------------
+    // ---- 4. ordinals, miss lists, locations ---------------------------------
     // Lane k < P: the first occurrences of the ranks below k (ranks P .. 7
     // add none); U, all of them.
     const int tot_k = lane < P ? s_tot[lane] : 0;
@@ -907,35 +932,35 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
             row[r] = code[r] >= 0 ? hrow[r] : (code[r] <= -3 ? phys[d.H + j[r]] : 0);
         if (tl && tid == 0) stamp_after(tl, TL_ROWS, row);
 #pragma unroll
+        for (int r = 0; r < RMAX; ++r) {  // first occurrences: list the miss
+            if (code[r] <= -3 &&
+                (miss_value(code[r]) & 0xffff) == c * kKeyStride + r * BD + tid) {
+                const int loc = (int)(base + row[r]);
+                a.ws.miss_tok[wbase + j[r]] = t[r];
+                a.ws.miss_last[wbase + j[r]] = miss_value(code[r]) >> 16;
+                a.ws.miss_dst[wbase + j[r]] = loc;
+                if (a.plan_src) {
+                    a.plan_src[wbase + j[r]] = (long long)q * d.L + t[r];
+                    a.plan_dst[wbase + j[r]] = loc;
+                }
+            }
+        }
+        // Last barrier, first half: the miss lists are written.  Inside it,
+        // the locations, which no CTA reads.
+        cluster_arrive();
+#pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             const int i = lo + r * BD + tid;
             if (i >= hi) continue;
-            int loc;
-            if ((xbits >> r) & 1u) {
+            int loc = code[r] == -1 ? -1 : (int)(base + row[r]);
+            if ((xbits >> r) & 1u)
                 loc = (int)((long long)d.R * (d.H + d.C) + (long long)q * d.E + t[r] % d.E);
-            } else if (code[r] >= 0) {
-                loc = (int)(base + row[r]);
-            } else if (code[r] == -1) {
-                loc = -1;
-            } else {
-                loc = (int)(base + row[r]);
-                if ((miss_value(code[r]) & 0xffff) == c * kKeyStride + r * BD + tid) {
-                    // first occurrence: list the miss
-                    a.ws.miss_tok[wbase + j[r]] = t[r];
-                    a.ws.miss_last[wbase + j[r]] = miss_value(code[r]) >> 16;
-                    a.ws.miss_dst[wbase + j[r]] = loc;
-                    if (a.plan_src) {
-                        a.plan_src[wbase + j[r]] = (long long)q * d.L + t[r];
-                        a.plan_dst[wbase + j[r]] = loc;
-                    }
-                }
-            }
             locs_b[i] = loc;
         }
     }
     // Miss lists visible to the whole cluster; no shared memory of another
     // CTA is touched after this point.
-    cluster.sync();
+    cluster_wait();
     if (tl && tid == 0) tl[TL_BARRIER_C] = global_timer();
     if (c == 0 && tid == 0) {
         int n_hit = 0, n_inv = 0, n_miss = 0, n_ext = 0;
