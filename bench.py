@@ -45,10 +45,10 @@ METRIC = "selected tokens resolved/s per layer-call"
 # profiles/swapin_kernel_traffic.md: DRAM read + write bytes and host-link
 # (system memory) read bytes.  Workloads without a capture of the current
 # kernel report null.
-NCU_TRAFFIC = {("C3", "dense"): {"dram_bytes": 17744128, "host_link_bytes": 41563595},
-               ("C2", "dense"): {"dram_bytes": 7468715, "host_link_bytes": 11190485},
-               ("C4", "dense"): {"dram_bytes": 1706240, "host_link_bytes": 22087371},
-               ("C5", "dense"): {"dram_bytes": 1963093, "host_link_bytes": 1695157}}
+NCU_TRAFFIC = {("C3", "dense"): {"dram_bytes": 17655637, "host_link_bytes": 41563818},
+               ("C2", "dense"): {"dram_bytes": 7480320, "host_link_bytes": 11190880},
+               ("C4", "dense"): {"dram_bytes": 1702570, "host_link_bytes": 22094272},
+               ("C5", "dense"): {"dram_bytes": 1972992, "host_link_bytes": 1695093}}
 NCU_CAPTURE = "profiles/swapin_kernel_traffic.md"
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
