@@ -39,8 +39,9 @@
 //   5. the leader CTA (rank 0) commits the request's policy state
 //      (epoch-CLOCK victims, admission, rotation, index update), while the
 //      other CTAs of the cluster copy the request's miss rows from the
-//      mapped pinned host pool, claiming 16-byte pieces from a per-batch-row
-//      counter; the leader joins the copy when it is done.  A cluster of one
+//      mapped pinned host pool in chunks of 16-byte pieces (each warp's
+//      first chunk by its index, the rest claimed from a per-batch-row
+//      counter); the leader joins the copy when it is done.  A cluster of one
 //      CTA commits on 16 of its warps and copies on the others.
 // A request's copy thus starts as soon as its own lookup is complete; no
 // CTA waits for another batch row.  The commit rewrites only policy state,
@@ -288,6 +289,14 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
     int* vict = reinterpret_cast<int*>(keys + H);  // victims in ascending slot order
     int32_t* adm = a.ws.adm + wbase;
 
+    // The request's use counters, read now so that their load is done by
+    // the time the commit updates them (nothing else writes them while the
+    // request is locked).
+    int used0 = 0, resident0 = 0;
+    if (tid == 0) {
+        used0 = ctrl[CTRL_USED];
+        resident0 = ctrl[CTRL_RESIDENT];
+    }
     // Keys for victim selection: epoch + 1 (0 = never used), or kHitKey for
     // a slot the call referenced, which takes epoch E in the same pass.
     // Each thread loads kKeyBatch epochs before it stores any, so the loads
@@ -463,8 +472,8 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
             fresh = both >> 16;
         }
         if (tid == 0) {
-            s_misc[0] = ctrl[CTRL_USED] + fresh;
-            s_misc[1] = ctrl[CTRL_RESIDENT] + m - evicted;
+            s_misc[0] = used0 + fresh;
+            s_misc[1] = resident0 + m - evicted;
         }
         g.sync();
         // ---- rebuild the bank once deleted entries pile up ---------------------
@@ -507,20 +516,30 @@ __device__ void commit_request(const SwapArgs& a, const Group& g, int b, int q, 
 // ---- copy (miss rows of one request) -----------------------------------------
 
 // Copies the U miss rows of one request (W bytes each) from its host pool
-// rows to their device rows, one warp at a time: a warp claims kWarpPieces
-// consecutive 16-byte pieces of the flattened (miss, piece) space from
-// `claim`, issues all its loads, then its stores, and claims again until
-// the pieces run out.  `mtok` and `mdst` were written earlier in this
-// kernel, so they are read with plain (coherent) loads.
+// rows to their device rows, one warp at a time: a warp takes kWarpPieces
+// consecutive 16-byte pieces of the flattened (miss, piece) space, issues
+// all its loads, then its stores, and takes more until the pieces run out.
+// The first `nfixed` chunks go to the warps that start copying at once, by
+// their index `fixed` (-1 for a warp that starts later), so that their first
+// loads wait for no atomic; every other chunk is claimed from `claim`.
+// `mtok` and `mdst` were written earlier in this kernel, so they are read
+// with plain (coherent) loads.
 __device__ void copy_request(const uint8_t* pool_q, uint8_t* kv, const int32_t* mtok,
-                             const int32_t* mdst, int U, int W, unsigned* claim) {
+                             const int32_t* mdst, int U, int W, unsigned* claim, int fixed,
+                             int nfixed) {
     const int lane = threadIdx.x & 31;
     const unsigned nv = (unsigned)W >> 4;  // 16-byte pieces per row
     const unsigned total = (unsigned)U * nv;
     for (;;) {
-        unsigned start = 0;
-        if (lane == 0) start = atomicAdd(claim, (unsigned)kWarpPieces);
-        start = __shfl_sync(0xffffffffu, start, 0);
+        unsigned start;
+        if (fixed >= 0) {
+            start = (unsigned)fixed * kWarpPieces;
+            fixed = -1;
+        } else {
+            start = 0;
+            if (lane == 0) start = atomicAdd(claim, (unsigned)kWarpPieces);
+            start = __shfl_sync(0xffffffffu, start, 0) + (unsigned)nfixed * kWarpPieces;
+        }
         if (start >= total) break;
         uint4 v[kCopyUnroll];
         long long dst[kCopyUnroll];  // destination byte offset of each piece, -1 if none
@@ -996,9 +1015,17 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
                        reinterpret_cast<unsigned*>(smem));
         if (tl && tid == 0) tl[TL_COMMITTED] = global_timer();
     }
-    if (!a.defer_copy && U > 0)
+    if (!a.defer_copy && U > 0) {
+        // Warps that copy from the start: every warp of the other CTAs (of
+        // all but the commit warps in a cluster of one); the leader's commit
+        // warps join when done.
+        const int nfixed = P > 1 ? (P - 1) * nwarps : nwarps - commit_warps;
+        const int fixed = P > 1 ? (c > 0 ? (c - 1) * nwarps + warp : -1)
+                                : (warp >= commit_warps ? warp - commit_warps : -1);
         copy_request(a.lv.host_pool + (long long)q * d.L * d.W, a.lv.device_kv,
-                     a.ws.miss_tok + wbase, a.ws.miss_dst + wbase, U, d.W, claim);
+                     a.ws.miss_tok + wbase, a.ws.miss_dst + wbase, U, d.W, claim, fixed,
+                     nfixed);
+    }
     if (tl && lane == 0 && atomicAdd(&s_done, 1) == nwarps - 1) tl[TL_COPIED] = global_timer();
 }
 
