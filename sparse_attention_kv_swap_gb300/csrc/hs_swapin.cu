@@ -16,26 +16,29 @@
 //      request's token -> slot index (dense map: one load; hash bank: linear
 //      probing with every first probe issued before any resolves);
 //   2. misses go into a de-duplication table spread over the cluster's
-//      shared memory, which keeps for each token the smallest flat index at
-//      which it occurs and the set of steps it occurs in.  When the table
+//      shared memory, which keeps for each token the smallest key (rank and
+//      local index, ordered as flat indices are) of the entries at which it
+//      occurs and the set of steps it occurs in.  When the table
 //      fits, it is indexed by the token's position (home CTA t mod P, entry
 //      t / P) and an insert is one fire-and-forget atomic (two in a
 //      multi-step call that may overflow); otherwise it is a hash table
 //      with linear probing (compare-and-swap inserts).  Step 1 touches no
-//      other CTA's shared memory, so it runs before the first cluster
-//      barrier; hit slots are marked in a shared-memory bitmap;
+//      other CTA's shared memory, so it runs inside the first cluster
+//      barrier; hit slots are marked in a shared-memory bitmap inside the
+//      second;
 //   3. an entry is the first occurrence of its token iff the table holds its
-//      own flat index.  Each CTA turns its first-occurrence flags into
-//      64-bit words (running count << 32 | flags of 32 entries) and sends
-//      them, its total, its entry counters and its hit bits to the other
-//      CTAs of the cluster (the hit bits to the leader only);
+//      own key.  Each CTA turns its first-occurrence flags into 64-bit words
+//      (running count << 32 | flags of 32 entries) and sends them and its
+//      total to every CTA of the cluster, its entry counters and hit bits to
+//      the leader;
 //   4. the ordinal j of a miss is the number of first occurrences before
 //      its token's first occurrence: the totals of lower-ranked CTAs plus
 //      that CTA's running count and flags up to it, all read from local
 //      shared memory.  Every entry gets its device row (q * (H + C) +
 //      phys[slot] for a hit, q * (H + C) + phys[H + j] for miss j,
 //      R * (H + C) + q * E + t mod E on the extra page); first occurrences
-//      list their token, last step and device row;
+//      list their token, last step and device row, and every location is
+//      stored inside the last cluster barrier;
 //   5. the leader CTA (rank 0) commits the request's policy state
 //      (epoch-CLOCK victims, admission, rotation, index update), while the
 //      other CTAs of the cluster copy the request's miss rows from the
@@ -591,11 +594,11 @@ __global__ void __launch_bounds__(1024, 1) swapin_kernel(const SwapArgs a) {
         tl[TL_CLUSTER_SIZE] = (unsigned long long)P;
     }
 
-    // This CTA's share of the de-duplication table, then the bitmap words.
-    // Indexed by position, an entry is the smallest flat index of the token
+    // This CTA's share of the de-duplication table, then the flag words.
+    // Indexed by position, an entry is the smallest entry key of the token
     // (int) and, when the call may overflow, the OR of its step bits next to
     // it (one 8-byte word, read by one load); hashed, the table keeps the
-    // tokens, the smallest flat indices and 8 step bits an entry apart.
+    // tokens, the smallest keys and 8 step bits an entry apart.
     // Only overflow admission reads a miss's last step, and a call with
     // S * K <= H cannot overflow: its distinct tokens, hits and misses
     // together, are at most S * K, so U <= H - #hit slots.
@@ -1140,7 +1143,7 @@ bool step_bits_needed(const Dims& d, int steps) {
 //     threads than entries would not pay: with one 1024-thread CTA per SM,
 //     clusters of 8 no longer all fit at once (16 of them in a 152-SM
 //     GB300 ran in two waves).
-//   - shared memory: the table share plus the bitmap words of every rank,
+//   - shared memory: the table share plus the flag words of every rank,
 //     or the commit's H keys and up to C victims if larger.
 SwapinShape swapin_shape(const Dims& d, int batch, int steps, int sms, int p_cap) {
     const int N = steps * d.K;
