@@ -45,10 +45,10 @@ METRIC = "selected tokens resolved/s per layer-call"
 # profiles/swapin_kernel_traffic.md: DRAM read + write bytes and host-link
 # (system memory) read bytes.  Workloads without a capture of the current
 # kernel report null.
-NCU_TRAFFIC = {("C3", "dense"): {"dram_bytes": 17779200, "host_link_bytes": 41563840},
-               ("C2", "dense"): {"dram_bytes": 7598506, "host_link_bytes": 11197866},
-               ("C4", "dense"): {"dram_bytes": 1700266, "host_link_bytes": 22087370},
-               ("C5", "dense"): {"dram_bytes": 1971968, "host_link_bytes": 1695306}}
+NCU_TRAFFIC = {("C3", "dense"): {"dram_bytes": 17851477, "host_link_bytes": 41563722},
+               ("C2", "dense"): {"dram_bytes": 7540650, "host_link_bytes": 11197845},
+               ("C4", "dense"): {"dram_bytes": 1712640, "host_link_bytes": 22087381},
+               ("C5", "dense"): {"dram_bytes": 1957632, "host_link_bytes": 1695200}}
 NCU_CAPTURE = "profiles/swapin_kernel_traffic.md"
 UNIT = "tokens/s"
 PREROLL_CALLS = 8  # calls of the stream run before warm-up so the cache is in steady state
