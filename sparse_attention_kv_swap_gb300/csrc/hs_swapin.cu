@@ -62,7 +62,7 @@ constexpr int kMaxCluster = 8;
 constexpr int kMissPending = -2;    // code of an entry that missed the index
 constexpr int kNoFirst = 0x7fffffff;  // de-duplication entry not yet seen
 constexpr int kCopyUnroll = 4;
-constexpr int kWarpPieces = 32 * kCopyUnroll;  // 16-byte pieces a warp claims at once
+constexpr int kWarpPieces = 32 * kCopyUnroll;  // 16-byte pieces a warp takes at once
 constexpr int kCommitWarps = 16;               // the leader CTA's commit warps (at most)
 constexpr unsigned kHitKey = 0xffffffffu;      // radix key of a slot referenced by the call
 constexpr int kKeyBatch = 8;                    // epochs a commit thread loads at once
